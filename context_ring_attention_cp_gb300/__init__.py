@@ -1,0 +1,208 @@
+"""Thin Python binding of ``libcpattn.so`` — argument marshalling only.
+
+Every function here has the name of the C-ABI entry point it calls
+(``include/cpattn.h``) and does nothing but turn tensors into pointers and
+sizes, pick the current CUDA stream, and raise :class:`CpError` on a non-OK
+status.  All computation happens in the library's CUDA kernels (or, for the
+planner and byte counts, in its host C++).  There is no fallback: if the
+library is missing this module raises on first use.
+
+PyTorch is used only for device memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE",
+    "CP_MAX_MERGE_PARTS", "library_path", "load_library", "cp_status_string",
+    "cp_plan_balanced_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn", "cp_merge_partials",
+    "cp_passq_workspace_bytes", "cp_passq_decode", "cp_take_device_status",
+]
+
+CP_OK = 0
+CP_ERR_INVALID_ARGUMENT = 1
+CP_ERR_UNSUPPORTED = 2
+CP_ERR_OVERFLOW = 3
+CP_ERR_CUDA = 4
+CP_ERR_TIMEOUT = 5
+CP_MODE_EMIT = 0
+CP_MODE_ACCUMULATE = 1
+CP_MODE_FINALIZE = 2
+CP_MAX_MERGE_PARTS = 256
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libcpattn.so")
+
+
+class CpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {cp_status_string(status)} ({status})")
+
+
+class AttnDesc(ctypes.Structure):
+    """Mirror of ``cp_attn_desc``."""
+    _fields_ = [("b", ctypes.c_int64), ("S", ctypes.c_int64), ("h_q", ctypes.c_int64),
+                ("h_kv", ctypes.c_int64), ("d", ctypes.c_int64), ("cp", ctypes.c_int64),
+                ("scale", ctypes.c_float), ("causal", ctypes.c_int32)]
+
+
+class _CommQuery(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("S", "cp", "c_kv", "b", "d", "n_h", "s_dtype")]
+
+
+class _CommResult(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("passkv_total", "passkv_per_step", "passq_dispatch",
+                                               "passq_reduce")]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+
+
+def load_library():
+    """Load ``libcpattn.so`` (it must have been built); raises if it is absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run __graft_entry__.build() (or "
+                           "python -m context_ring_attention_cp_gb300._build) first")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "cp_status_string": (ctypes.c_char_p, [_I32]),
+        "cp_plan_balanced_chunks": (_I32, [_I64, _I32, _P, _P, _P, _P]),
+        "cp_comm_bytes": (_I32, [ctypes.POINTER(_CommQuery), ctypes.POINTER(_CommResult)]),
+        "cp_ring_step_partial_attn": (_I32, [ctypes.POINTER(AttnDesc), _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                             _I32, _P]),
+        "cp_merge_partials": (_I32, [_I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _P]),
+        "cp_passq_workspace_bytes": (_I32, [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]),
+        "cp_passq_decode": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P]),
+        "cp_take_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    """Device address of a tensor (or an int address, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != CP_OK:
+        raise CpError(status, where)
+
+
+def cp_status_string(status: int) -> str:
+    return load_library().cp_status_string(int(status)).decode()
+
+
+def make_desc(b, S, h_q, h_kv, d, cp, scale, causal) -> AttnDesc:
+    return AttnDesc(int(b), int(S), int(h_q), int(h_kv), int(d), int(cp), float(scale), int(causal))
+
+
+def cp_plan_balanced_chunks(S: int, cp: int) -> dict:
+    """Host planner; returns the four plan arrays as numpy arrays."""
+    lib = load_library()
+    if not isinstance(cp, (int, np.integer)) or cp < 1 or cp > (1 << 20):
+        # the arrays below are sized by cp: reject before allocating (the library checks again)
+        raise CpError(CP_ERR_INVALID_ARGUMENT, "cp_plan_balanced_chunks")
+    chunk_begin = np.zeros(2 * cp + 1, np.int64)
+    rank_chunks = np.zeros((cp, 2), np.int32)
+    step_src = np.zeros((cp, cp), np.int32)
+    step_pairs = np.zeros((cp, cp), np.int64)
+    st = lib.cp_plan_balanced_chunks(int(S), int(cp), chunk_begin.ctypes.data, rank_chunks.ctypes.data,
+                                     step_src.ctypes.data, step_pairs.ctypes.data)
+    _check(st, "cp_plan_balanced_chunks")
+    return {"chunk_begin": chunk_begin, "rank_chunks": rank_chunks, "step_src": step_src,
+            "step_pairs": step_pairs}
+
+
+def cp_comm_bytes(S, cp, c_kv, b=0, d=0, n_h=0, s_dtype=0) -> dict:
+    """Closed-form pass-KV / pass-Q byte counts (host, exact uint64)."""
+    lib = load_library()
+    q = _CommQuery(int(S), int(cp), int(c_kv), int(b), int(d), int(n_h), int(s_dtype))
+    r = _CommResult()
+    _check(lib.cp_comm_bytes(ctypes.byref(q), ctypes.byref(r)), "cp_comm_bytes")
+    return {"passkv_total": int(r.passkv_total), "passkv_per_step": int(r.passkv_per_step),
+            "passq_dispatch": int(r.passq_dispatch), "passq_reduce": int(r.passq_reduce)}
+
+
+def cp_ring_step_partial_attn(desc: AttnDesc, step_begin: int, step_end: int, q, k, v, o, m, l,
+                              mode: int = CP_MODE_EMIT, stream=None) -> None:
+    """Ring steps [step_begin, step_end) for all virtual ranks (see include/cpattn.h)."""
+    lib = load_library()
+    st = lib.cp_ring_step_partial_attn(ctypes.byref(desc), int(step_begin), int(step_end), _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(o), _ptr(m), _ptr(l), int(mode), _stream(stream))
+    _check(st, "cp_ring_step_partial_attn")
+
+
+def cp_merge_partials(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out,
+                      order=None, finalize=False, stream=None) -> None:
+    """LSE merge of n_parts triples in ``order`` (a host sequence, or None for index order)."""
+    lib = load_library()
+    order_arr = None
+    order_ptr = None
+    if order is not None:
+        order_arr = np.ascontiguousarray(np.asarray(order, dtype=np.int32))
+        if order_arr.size != int(n_parts):
+            raise CpError(CP_ERR_INVALID_ARGUMENT, "cp_merge_partials")
+        order_ptr = order_arr.ctypes.data
+    st = lib.cp_merge_partials(int(batch), int(rows), int(heads), int(d), int(n_parts), _ptr(o_parts),
+                               _ptr(m_parts), _ptr(l_parts), order_ptr, _ptr(o_out), _ptr(m_out), _ptr(l_out),
+                               int(bool(finalize)), _stream(stream))
+    _check(st, "cp_merge_partials")
+
+
+def cp_passq_workspace_bytes(desc: AttnDesc) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib.cp_passq_workspace_bytes(ctypes.byref(desc), ctypes.byref(n)), "cp_passq_workspace_bytes")
+    return int(n.value)
+
+
+def cp_passq_decode(desc: AttnDesc, q, k, v, workspace, workspace_bytes: int, out, m_out=None, l_out=None,
+                    stream=None) -> None:
+    """Pass-Q decode: partials over cp shards, then the LSE reduce into ``out``."""
+    lib = load_library()
+    st = lib.cp_passq_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(workspace),
+                             int(workspace_bytes), _ptr(out), _ptr(m_out), _ptr(l_out), _stream(stream))
+    _check(st, "cp_passq_decode")
+
+
+def cp_take_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word."""
+    lib = load_library()
+    s = _I32(0)
+    _check(lib.cp_take_device_status(_stream(stream), ctypes.byref(s)), "cp_take_device_status")
+    return int(s.value)

@@ -1,0 +1,49 @@
+// Internal interface between the C-ABI layer (capi.cpp) and the kernel files.
+// Every function here is called only after capi.cpp has validated its arguments.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+// ---- LSE merge (merge.cu) --------------------------------------------------
+struct MergeParams {
+  int64_t batch, rows, heads, d;
+  int32_t n_parts;
+  int32_t finalize;
+  const float* o_parts;
+  const float* m_parts;
+  const float* l_parts;
+  float* o_out;
+  float* m_out;  // may be null
+  float* l_out;  // may be null
+  uint16_t order[CP_MAX_MERGE_PARTS];  // fold order (a permutation of 0..n_parts-1)
+};
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+// ---- pass-Q decode partials (decode.cu) ------------------------------------
+// Key ranges per shard chosen for the device's SM count; n_parts = cp * splits.
+int32_t decode_splits_per_shard(const cp_attn_desc& d, int sm_count);
+size_t decode_workspace_bytes(const cp_attn_desc& d, int32_t splits);
+// Splits the workspace into O partials [n_parts, b, h_q, d], then m and l [n_parts, b, h_q],
+// each section starting on a 16-byte boundary.
+void decode_workspace_sections(const cp_attn_desc& d, int32_t splits, float* ws, float** o_parts,
+                               float** m_parts, float** l_parts);
+bool decode_supported(const cp_attn_desc& d);
+cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const void* q,
+                                   const void* k, const void* v, float* o_parts,
+                                   float* m_parts, float* l_parts, cudaStream_t stream);
+
+// ---- ring-step attention (ring_attn.cu) ------------------------------------
+bool ring_supported(const cp_attn_desc& d);
+// Returns CP_OK, or CP_ERR_CUDA when a tensor map cannot be encoded or the launch fails.
+cp_status launch_ring_attn(const cp_attn_desc& d, int32_t step_begin, int32_t step_end,
+                           const void* q, const void* k, const void* v, float* o, float* m,
+                           float* l, int32_t mode, cudaStream_t stream);
+// Reads and clears the ring kernel's device status word (after the caller synchronised).
+cudaError_t ring_take_status(int32_t* status);
+
+}  // namespace cpattn

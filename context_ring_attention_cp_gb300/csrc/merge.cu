@@ -1,0 +1,174 @@
+// LSE merge of partial attention triples (the "three-quantity reduce").
+//
+// "G5 上下文并行建模设计规格", Terms table, row "Partial attention": the triple
+// (max / numerator / denominator) of disjoint key sets merges associatively and
+// in any order.  For parts p taken in the caller's order:
+//   m = max_p m_p,  l = sum_p e^{m_p - m} l_p,  O = sum_p e^{m_p - m} O_p.
+// Taking m first (exact, order-free) and then summing the weighted parts is the
+// same quantity as a left fold of pairwise merges; only rounding differs.
+//
+// HBM-bound: each (batch, head, row) reads n_parts x (d + 2) floats and writes
+// d + 2.  One CTA covers 32 consecutive rows of one (batch, head): it first
+// stages the 2 x n_parts x 32 scalars (m, l) with coalesced loads into shared
+// memory, then each warp streams the O rows of its rows part by part, lanes
+// owning float4 slices of d, with eight (d <= 128) down to two (d = 512) parts of loads
+// in flight per lane.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kRowsPerCta = 32;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <int NCH>  // float4 slices of d owned by one lane (d <= 128 * NCH)
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ MergeParams p) {
+  constexpr int kUnroll = (8 / NCH) < 2 ? 2 : (8 / NCH);  // parts in flight per lane
+  extern __shared__ float smem[];
+  const int n_parts = p.n_parts;
+  float* sm_m = smem;                          // [n_parts][32] in fold order
+  float* sm_l = smem + n_parts * kRowsPerCta;  // [n_parts][32]
+
+  const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t tile = blockIdx.x;
+  const int64_t rb = tile % row_blocks;
+  const int64_t bh = tile / row_blocks;  // batch * heads + head
+  const int64_t h = bh % p.heads;
+  const int64_t bi = bh / p.heads;
+  const int64_t row0 = rb * kRowsPerCta;
+
+  // Stage m and l of every part for the 32 rows (consecutive threads -> consecutive rows).
+  for (int idx = threadIdx.x; idx < n_parts * kRowsPerCta; idx += kThreads) {
+    const int kpos = idx / kRowsPerCta;
+    const int r = idx % kRowsPerCta;
+    const int part = p.order[kpos];
+    const int64_t row = row0 + r;
+    float mv = -INFINITY, lv = 0.f;
+    if (row < p.rows) {
+      const int64_t off = ((int64_t(part) * p.batch + bi) * p.heads + h) * p.rows + row;
+      mv = p.m_parts[off];
+      lv = p.l_parts[off];
+    }
+    sm_m[idx] = mv;
+    sm_l[idx] = lv;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int64_t n_vec = p.d / 4;
+  const int64_t part_stride = p.batch * p.rows * p.heads * p.d;  // floats between parts of O
+
+  for (int r = warp; r < kRowsPerCta; r += kWarps) {
+    const int64_t row = row0 + r;
+    if (row >= p.rows) break;
+    // m = max over parts (exact in any order).
+    float mx = -INFINITY;
+    for (int kpos = lane; kpos < n_parts; kpos += 32) mx = fmaxf(mx, sm_m[kpos * kRowsPerCta + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    // All parts the identity: the row stays the identity (never NaN).
+    const float shift = (mx == -INFINITY) ? 0.f : mx;
+
+    float lsum = 0.f;
+    float4 acc[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t obase = ((bi * p.rows + row) * p.heads + h) * p.d;
+
+    for (int k0 = 0; k0 < n_parts; k0 += kUnroll) {
+      float4 x[kUnroll][NCH];
+      float w[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int kpos = k0 + u;
+        const bool ok = kpos < n_parts;
+        const int part = ok ? p.order[kpos] : 0;
+        w[u] = ok ? expf(sm_m[kpos * kRowsPerCta + r] - shift) : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(p.o_parts + int64_t(part) * part_stride + obase);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int64_t vi = lane + 32 * c;
+          x[u][c] = (ok && vi < n_vec) ? ld_stream(src + vi) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int kpos = k0 + u;
+        if (kpos < n_parts) lsum = fmaf(w[u], sm_l[kpos * kRowsPerCta + r], lsum);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          acc[c].x = fmaf(w[u], x[u][c].x, acc[c].x);
+          acc[c].y = fmaf(w[u], x[u][c].y, acc[c].y);
+          acc[c].z = fmaf(w[u], x[u][c].z, acc[c].z);
+          acc[c].w = fmaf(w[u], x[u][c].w, acc[c].w);
+        }
+      }
+    }
+    const float inv = (p.finalize && lsum > 0.f) ? 1.f / lsum : 1.f;
+    const bool zero = p.finalize && !(lsum > 0.f);
+    float4* dst = reinterpret_cast<float4*>(p.o_out + obase);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int64_t vi = lane + 32 * c;
+      if (vi < n_vec) {
+        float4 y = acc[c];
+        if (zero) {
+          y = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (p.finalize) {
+          y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
+        }
+        dst[vi] = y;
+      }
+    }
+    if (lane == 0) {
+      const int64_t off = (bi * p.heads + h) * p.rows + row;
+      if (p.m_out) p.m_out[off] = mx;
+      if (p.l_out) p.l_out[off] = lsum;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t tiles = row_blocks * p.batch * p.heads;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const size_t smem = size_t(2) * p.n_parts * kRowsPerCta * sizeof(float);
+  const int nch = int((p.d / 4 + 31) / 32);
+  cudaError_t e = cudaSuccess;
+  switch (nch) {
+#define CP_MERGE_CASE(N)                                                                       \
+  case N:                                                                                      \
+    e = cudaFuncSetAttribute(lse_merge_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             int(smem));                                                       \
+    if (e != cudaSuccess) return e;                                                            \
+    lse_merge_kernel<N><<<unsigned(tiles), kThreads, smem, stream>>>(p);                       \
+    break;
+    CP_MERGE_CASE(1)
+    CP_MERGE_CASE(2)
+    CP_MERGE_CASE(3)
+    CP_MERGE_CASE(4)
+#undef CP_MERGE_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -1,0 +1,776 @@
+// Ring-step partial attention for all cp virtual ranks, on sm_103a tensor cores.
+//
+// Method ("G5 上下文并行建模设计规格", G5 CP modelling spec):
+//  * Terms table, "Balanced chunk split": the sequence is cut into 2*cp chunks of
+//    C tokens; rank r owns chunk r (head) and chunk 2cp-1-r (tail).
+//  * Terms table, "Pass-KV" / "Ring step": in step t rank r computes partial
+//    attention of its rows against the K/V block it holds, the block of source
+//    rank s = (r - t) mod cp.  On one GPU the rotation is an index change: the
+//    kernel reads the source rank's chunks straight from HBM.
+//  * Terms table, "Partial attention": each step yields the online-softmax
+//    triple (max m, denominator l, numerator O); triples merge associatively.
+//  * eq. g5cp-step-flops: every (rank, step) holds the same 2*C^2 visible pairs
+//    (plus C on step 0), F_attn / cp^2.
+//
+// Work decomposition.  One CTA owns one 128-row query tile of one chunk for up
+// to two query heads that share a kv head (grouped-query attention), and walks
+// the ring steps [step_begin, step_end) in order.  For each step it visits the
+// 128-key tiles of the source rank's two chunks that its rows can see: chunks
+// before the query chunk are fully visible, the query chunk itself (step 0 only)
+// is the causal diagonal, later chunks are skipped.  The running triple stays on
+// chip across all steps, so the between-step merge is the online-softmax update
+// itself; the epilogue emits the triple, or merges it into the triple already in
+// HBM, and optionally normalises.  CTAs are ordered latest-chunk first (longest
+// first), and the hardware block scheduler hands them out as SMs free up.
+//
+// Per CTA (384 threads, one CTA per SM):
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of smem slots
+//   warp 1      TMEM owner and MMA issuer (one lane): S = Q K^T and O += P V
+//   warps 4-7   softmax of query tile A (thread = row = TMEM lane)
+//   warps 8-11  softmax of query tile B
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B.  P (bf16)
+// is written over the first 64 columns of its S tile and fed to the PV MMA from
+// TMEM.  The MMA warp issues PV_T(j) before S_T(j+1), and tcgen05.mma executes in
+// issue order, so P_T(j) is consumed before S_T(j+1) overwrites it.  The commit
+// that signals S_T(j+1) also covers PV_T(j), so softmax may rescale O_T then.
+//
+// Softmax runs in base 2 on logits scaled by scale*log2(e).  The reference max
+// used for the exponent is only raised when the row max grows by more than 8
+// (a factor 256): the triple (m_ref, l, O) stays exact, P <= 256 fits bf16, and
+// O is rescaled in TMEM only on those rare raises.  The true max is tracked on
+// the side and the epilogue re-expresses (l, O) against it, so the stored m is
+// the definition's max.
+//
+// Every mbarrier wait is bounded (about 1 s); on expiry the CTA records
+// CP_ERR_TIMEOUT in a device status word, every role bails out, in-flight async
+// copies are given time to land, TMEM is freed and the CTA returns.  While that
+// word holds an error, CTAs of later launches return at once without writing
+// (the outputs are undefined until cp_take_device_status clears it).
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // keys per KV tile
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+
+__device__ int32_t g_ring_status = 0;
+
+template <int D>
+struct Cfg {
+  static constexpr int kSlab = BM * 128;             // bytes of one 64-column swizzled slab
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kTileBytes = BM * D * 2;      // Q tile, K tile and V tile alike
+  static constexpr int kStages = (D == 128) ? 4 : 6;
+  static constexpr int kQOff = 0;
+  static constexpr int kKvOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 1024 + 1024;  // barriers/flags + alignment slack
+  static constexpr uint32_t kOCol = 256;
+};
+
+struct RingParams {
+  CUtensorMap tmap_q;  // dims (d, h_q, S, b)
+  CUtensorMap tmap_k;  // dims (d, h_kv, S, b)
+  CUtensorMap tmap_v;
+  float* o;
+  float* m;
+  float* l;
+  int64_t b, S, h_q, h_kv;
+  int32_t C;          // chunk length S / (2 cp)
+  int32_t cp;
+  int32_t tpc;        // query tiles per chunk
+  int32_t n_pairs;    // head pairs per batch entry
+  int32_t ppg;        // head pairs per kv group
+  int32_t group;      // h_q / h_kv
+  int32_t step_begin, step_end;
+  int32_t mode;
+  float sl;           // scale * log2(e)
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false when the CTA has aborted or this wait timed out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        atomicExch(&g_ring_status, int32_t(CP_ERR_TIMEOUT));
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((addr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator, M = 128.
+__host__ __device__ constexpr uint32_t instr_desc(int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | (uint32_t(n >> 3) << 17) |
+         (uint32_t(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Wait for this thread's TMEM loads; the registers pass through so no use of
+// them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                 "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Ring schedule: the KV tiles one query tile visits over steps [t0, t1)
+// ---------------------------------------------------------------------------
+
+struct KvCursor {
+  int32_t cp, r, c_q, t, t_end, half;
+  int32_t C, q_last;
+  int32_t seg_key0, seg_n, seg_end, seg_i;
+  bool seg_diag;
+
+  __device__ void init(int32_t cp_, int32_t r_, int32_t c_q_, int32_t t0, int32_t t1, int32_t C_,
+                       int32_t q_last_) {
+    cp = cp_; r = r_; c_q = c_q_; t = t0; t_end = t1; half = 0;
+    C = C_; q_last = q_last_;
+    seg_key0 = seg_n = seg_end = seg_i = 0;
+    seg_diag = false;
+  }
+
+  // Next non-empty chunk segment: per step the head chunk of the source rank,
+  // then its tail chunk.
+  __device__ void find() {
+    seg_n = 0;
+    while (t < t_end) {
+      const int32_t s = ((r - t) % cp + cp) % cp;
+      const int32_t c = (half == 0) ? s : 2 * cp - 1 - s;
+      half ^= 1;
+      if (half == 0) ++t;
+      seg_i = 0;
+      seg_key0 = c * C;
+      seg_end = (c + 1) * C;
+      if (c < c_q) {
+        seg_diag = false;
+        seg_n = (C + BN - 1) / BN;
+        return;
+      }
+      if (c == c_q) {
+        seg_diag = true;
+        seg_n = (q_last - c * C) / BN + 1;
+        return;
+      }
+    }
+  }
+
+  __device__ bool next(int32_t& key0, int32_t& key_end, bool& diag) {
+    if (seg_i >= seg_n) {
+      find();
+      if (seg_n == 0) return false;
+    }
+    key0 = seg_key0 + BN * seg_i;
+    key_end = seg_end;
+    diag = seg_diag;
+    ++seg_i;
+    return true;
+  }
+};
+
+struct Item {
+  int32_t bi, h0, has_b, kvh;
+  int32_t c_q, r, q_row0, q_rows;
+};
+
+__device__ __forceinline__ Item decode_item(const RingParams& p) {
+  Item it;
+  const int32_t n_qt = 2 * p.cp * p.tpc;
+  const int64_t per_tile = p.b * p.n_pairs;
+  const int64_t idx = blockIdx.x;
+  const int32_t gq = n_qt - 1 - int32_t(idx / per_tile);  // latest chunk (most keys) first
+  const int64_t bp = idx % per_tile;
+  const int32_t pair = int32_t(bp % p.n_pairs);
+  it.bi = int32_t(bp / p.n_pairs);
+  it.kvh = pair / p.ppg;
+  const int32_t i = pair % p.ppg;
+  it.h0 = it.kvh * p.group + 2 * i;
+  it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
+  it.c_q = gq / p.tpc;
+  const int32_t kq = gq % p.tpc;
+  it.q_row0 = it.c_q * p.C + BM * kq;
+  it.q_rows = min(BM, p.C - BM * kq);
+  it.r = (it.c_q < p.cp) ? it.c_q : 2 * p.cp - 1 - it.c_q;
+  return it;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_constant__ RingParams p) {
+  using K = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::kBarOff);
+  // barrier slots
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  auto bar_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto bar_empty = [&](int s) { return smem_u32(&bars[1 + K::kStages + s]); };
+  auto bar_s = [&](int tt) { return smem_u32(&bars[1 + 2 * K::kStages + tt]); };
+  auto bar_p = [&](int tt) { return smem_u32(&bars[3 + 2 * K::kStages + tt]); };
+  auto bar_o = [&](int tt) { return smem_u32(&bars[5 + 2 * K::kStages + tt]); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[8 + 2 * K::kStages]);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const Item it = decode_item(p);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < K::kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int tt = 0; tt < 2; ++tt) {
+      mbar_init(bar_s(tt), 1);
+      mbar_init(bar_p(tt), BM);
+      mbar_init(bar_o(tt), 1);
+    }
+    // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) ? 1 : 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+
+  // Number of KV tiles this query tile visits over the step range.
+  int32_t n_kv = 0;
+  {
+    KvCursor cur;
+    cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
+    int32_t k0, ke;
+    bool dg;
+    while (cur.next(k0, ke, dg)) ++n_kv;
+  }
+  const int n_q = 1 + it.has_b;
+
+  // Register split (launched with 168 per thread, 64,512 in all): the producer /
+  // MMA warpgroup gives registers to the two softmax warpgroups.
+  // 128 x 56 + 256 x 216 = 62,464 <= 64,512, so the increase never waits.  Each
+  // role's code is reachable only after its own setmaxnreg; the common tail is tiny.
+  if (skip) {
+    // nothing to do: fall through to the teardown
+  } else if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kv > 0) {
+      mbar_expect_tx(bar_q, uint32_t(n_q * K::kTileBytes));
+      for (int tt = 0; tt < n_q; ++tt)
+        for (int sl = 0; sl < K::kSlabs; ++sl)
+          tma_load_4d(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
+                      it.h0 + tt, it.q_row0, it.bi);
+      KvCursor cur;
+      cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
+      int32_t key0, key_end;
+      bool diag;
+      int32_t li = 0;  // load index: K_j = 2j, V_j = 2j + 1
+      bool ok = true;
+      while (ok && cur.next(key0, key_end, diag)) {
+        for (int which = 0; which < 2 && ok; ++which, ++li) {
+          const int s = li % K::kStages;
+          const int round = li / K::kStages;
+          if (round > 0 && !mbar_wait(bar_empty(s), uint32_t((round - 1) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar_full(s), uint32_t(K::kTileBytes));
+          const CUtensorMap* map = which == 0 ? &p.tmap_k : &p.tmap_v;
+          for (int sl = 0; sl < K::kSlabs; ++sl)
+            tma_load_4d(sbase + K::kKvOff + s * K::kTileBytes + sl * K::kSlab, map, bar_full(s), sl * 64, it.kvh,
+                        key0, it.bi);
+        }
+      }
+      if (!ok) {  // let copies in flight land before the CTA can exit
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t idesc_s = instr_desc(BN, false);
+      constexpr uint32_t idesc_pv = instr_desc(D, true);
+      const uint32_t s_col[2] = {0u, 128u};
+      const uint32_t o_col[2] = {K::kOCol, K::kOCol + uint32_t(D)};
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      auto issue_s = [&](int tt, int slot) {
+        const uint32_t qa = sbase + K::kQOff + tt * K::kTileBytes;
+        const uint32_t ka = sbase + K::kKvOff + slot * K::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * K::kSlab + (kk % 4) * 32;
+          mma_ss(tmem + s_col[tt], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int tt, int slot, bool accumulate) {
+        const uint32_t va = sbase + K::kKvOff + slot * K::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_ts(tmem + o_col[tt], tmem + s_col[tt] + uint32_t(kk * 8), smem_desc(va + kk * 2048, K::kSlab, 1024),
+                 idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      // prologue: S(0) for both tiles
+      if (ok) ok = mbar_wait(bar_full(0), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int tt = 0; tt < n_q; ++tt) {
+          issue_s(tt, 0);
+          mma_commit(bar_s(tt));
+        }
+        mma_commit(bar_empty(0));
+      }
+      for (int32_t j = 0; ok && j < n_kv; ++j) {
+        const int lv = 2 * j + 1, lk = 2 * j + 2;
+        const int sv = lv % K::kStages, sk = lk % K::kStages;
+        if (!mbar_wait(bar_full(sv), uint32_t((lv / K::kStages) & 1), abort_flag)) { ok = false; break; }
+        const bool more = (j + 1 < n_kv);
+        bool k_ready = false;
+        for (int tt = 0; tt < n_q; ++tt) {
+          if (!mbar_wait(bar_p(tt), uint32_t(j & 1), abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(tt, sv, j > 0);
+          if (tt == n_q - 1) mma_commit(bar_empty(sv));  // V_j consumed by every tile
+          if (more) {
+            if (!k_ready) {
+              if (!mbar_wait(bar_full(sk), uint32_t((lk / K::kStages) & 1), abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(tt, sk);
+            mma_commit(bar_s(tt));
+            if (tt == n_q - 1) mma_commit(bar_empty(sk));  // K_{j+1} consumed
+          } else {
+            mma_commit(bar_o(tt));
+          }
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 50000ull) {
+        }
+      }
+    }
+  }
+  } else {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
+  if (warp < 8 || it.has_b) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int tt = (warp - 4) / 4;
+    const int t = threadIdx.x - 128 * (1 + tt);  // row within the tile == TMEM lane
+    const int h = it.h0 + tt;
+    const int32_t row = it.q_row0 + t;
+    const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + uint32_t(tt * 128);
+    const uint32_t o_addr = tmem + lane_base + K::kOCol + uint32_t(tt * D);
+    float m_ref = -INFINITY;   // exponent reference (log2 units)
+    float m_true = -INFINITY;  // true running max (log2 units)
+    float l_run = 0.f;
+    bool ok = true;
+
+    KvCursor cur;
+    cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
+    for (int32_t j = 0; j < n_kv; ++j) {
+      int32_t key0 = 0, key_end = 0;
+      bool diag = false;
+      cur.next(key0, key_end, diag);
+      // Warp-uniform outcome: the TMEM accesses below are warp-collective.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s(tt), uint32_t(j & 1), abort_flag))) { ok = false; break; }
+      tc_fence_after();
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + uint32_t(c * 32), r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.sl;
+      }
+      const bool full = (key0 + BN <= key_end) && (!diag || key0 + BN - 1 <= it.q_row0);
+      if (!full) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int32_t key = key0 + i;
+          const bool vis = key < key_end && (!diag || key <= row);
+          x[i] = vis ? x[i] : -INFINITY;
+        }
+      }
+      float tmax = x[0];
+#pragma unroll
+      for (int i = 1; i < BN; ++i) tmax = fmaxf(tmax, x[i]);
+      m_true = fmaxf(m_true, tmax);
+      // Raise the exponent reference only when the max grew by more than the threshold.
+      const bool raise = tmax > m_ref + kRescaleThreshold;
+      const float m_new = raise ? tmax : m_ref;
+      const float corr = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - m_new);
+      const bool rescale_o = raise && j > 0 && m_ref != -INFINITY;
+      if (raise) {
+        l_run *= corr;
+        m_ref = m_new;
+      }
+      const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = ex2(x[c * 32 + 2 * i] - mu);
+          const float b = ex2(x[c * 32 + 2 * i + 1] - mu);
+          psum += a + b;
+          pk[i] = pack_bf16(a, b);
+        }
+        tmem_st16(s_addr + uint32_t(c * 16), pk);
+      }
+      l_run += psum;
+      // O is rescaled after P is out (the logits are dead by then); PV_T(j)
+      // cannot start before this thread's arrive below.
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        const float f = rescale_o ? corr : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + uint32_t(c * 32), r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+          tmem_st32(o_addr + uint32_t(c * 32), r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p(tt));
+    }
+
+    // ---------------- epilogue: this row's triple, merged / normalised as asked
+    const bool have = ok && n_kv > 0;
+    if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), 0, abort_flag))) ok = false;
+    if (ok) {
+      tc_fence_after();
+      // Re-express (l, O) against the true max: factor 2^(m_ref - m_true) <= 1.
+      const float fre = (m_true == -INFINITY) ? 0.f : ex2(m_ref - m_true);
+      const float m_new_nat = m_true * kLn2;
+      const float l_new = l_run * fre;
+      const bool row_ok = t < it.q_rows && row < p.S;
+      const int64_t ml_off = (int64_t(it.bi) * p.h_q + h) * p.S + row;
+      float alpha = 0.f, beta = 1.f, l_out = l_new, m_out = m_new_nat;
+      if ((p.mode & CP_MODE_ACCUMULATE) && row_ok) {
+        const float m_old = p.m[ml_off];
+        const float l_old = p.l[ml_off];
+        m_out = fmaxf(m_old, m_new_nat);
+        const float sh = (m_out == -INFINITY) ? 0.f : m_out;
+        alpha = __expf(m_old - sh);
+        beta = __expf(m_new_nat - sh);
+        l_out = alpha * l_old + beta * l_new;
+      }
+      const bool fin = (p.mode & CP_MODE_FINALIZE) != 0;
+      const float inv = (fin && l_out > 0.f) ? 1.f / l_out : (fin ? 0.f : 1.f);
+      const float wnew = beta * fre * inv;
+      const float wold = alpha * inv;
+      float* orow = p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (have) {
+          tmem_ld32(o_addr + uint32_t(c * 32), r);
+          tmem_ld_wait(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v;
+            v.x = __uint_as_float(r[i]) * wnew;
+            v.y = __uint_as_float(r[i + 1]) * wnew;
+            v.z = __uint_as_float(r[i + 2]) * wnew;
+            v.w = __uint_as_float(r[i + 3]) * wnew;
+            if (p.mode & CP_MODE_ACCUMULATE) {
+              const float4 old = *reinterpret_cast<const float4*>(orow + c * 32 + i);
+              v.x = fmaf(old.x, wold, v.x);
+              v.y = fmaf(old.y, wold, v.y);
+              v.z = fmaf(old.z, wold, v.z);
+              v.w = fmaf(old.w, wold, v.w);
+            }
+            *reinterpret_cast<float4*>(orow + c * 32 + i) = v;
+          }
+        }
+      }
+      if (row_ok) {
+        p.m[ml_off] = m_out;
+        p.l[ml_off] = l_out;
+      }
+    }
+  }
+
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) !=
+            cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 4-D bf16 map over a [b, S, h, d] tensor: dims (d, h, S, b), box (64, 1, 128, 1), 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_t h, int64_t d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(h), cuuint64_t(S), cuuint64_t(b)};
+  const cuuint64_t strides[3] = {cuuint64_t(d * 2), cuuint64_t(h * d * 2), cuuint64_t(S * h * d * 2)};
+  const cuuint32_t box[4] = {64, 1, BM, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
+  using K = Cfg<D>;
+  if (cudaFuncSetAttribute(ring_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes) !=
+      cudaSuccess)
+    return CP_ERR_CUDA;
+  ring_attn_kernel<D><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
+}  // namespace
+
+bool ring_supported(const cp_attn_desc& d) {
+  // Keys and rows are indexed with int32 inside the kernel.
+  return (d.d == 64 || d.d == 128) && d.S < (int64_t(1) << 30) && d.b <= 65535 && d.h_q <= 65535;
+}
+
+cp_status launch_ring_attn(const cp_attn_desc& d, int32_t step_begin, int32_t step_end, const void* q,
+                           const void* k, const void* v, float* o, float* m, float* l, int32_t mode,
+                           cudaStream_t stream) {
+  RingParams p;
+  memset(&p, 0, sizeof(p));
+  if (!encode_map(&p.tmap_q, q, d.b, d.S, d.h_q, d.d) || !encode_map(&p.tmap_k, k, d.b, d.S, d.h_kv, d.d) ||
+      !encode_map(&p.tmap_v, v, d.b, d.S, d.h_kv, d.d))
+    return CP_ERR_CUDA;
+  p.o = o;
+  p.m = m;
+  p.l = l;
+  p.b = d.b;
+  p.S = d.S;
+  p.h_q = d.h_q;
+  p.h_kv = d.h_kv;
+  p.cp = int32_t(d.cp);
+  p.C = int32_t(d.S / (2 * d.cp));
+  p.tpc = (p.C + BM - 1) / BM;
+  p.group = int32_t(d.h_q / d.h_kv);
+  p.ppg = (p.group + 1) / 2;
+  p.n_pairs = int32_t(d.h_kv) * p.ppg;
+  p.step_begin = step_begin;
+  p.step_end = step_end;
+  p.mode = mode;
+  p.sl = d.scale * kLog2e;
+  const int64_t n_items = int64_t(2) * p.cp * p.tpc * d.b * p.n_pairs;
+  if (n_items > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
+  return d.d == 128 ? launch_d<128>(p, n_items, stream) : launch_d<64>(p, n_items, stream);
+}
+
+cudaError_t ring_take_status(int32_t* status) {
+  int32_t s = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&s, g_ring_status, sizeof(s));
+  if (e != cudaSuccess) return e;
+  const int32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_ring_status, &zero, sizeof(zero));
+  *status = s;
+  return e;
+}
+
+}  // namespace cpattn

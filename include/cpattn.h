@@ -1,0 +1,213 @@
+/*
+ * cpattn.h — C ABI of the GB300 (sm_103a) context-parallel ring-attention library.
+ *
+ * The operations follow the page "G5 上下文并行建模设计规格" (G5 context-parallel
+ * modelling design spec, v1.1.1).  The cp ranks of that spec are VIRTUAL ranks
+ * that all live on one GPU: the pass-KV rotation is an index change (rank r at
+ * ring step t reads the K/V rows of source rank s = (r - t) mod cp straight from
+ * HBM) and the pass-Q dispatch is a shared buffer.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Ownership: the caller allocates and owns every buffer and the CUDA stream.
+ *   The library never allocates device memory, never frees, keeps no state
+ *   between calls except the device status word read by
+ *   cp_take_device_status(), and never synchronises a stream (except in
+ *   cp_take_device_status()).  Device calls are asynchronous on `cuda_stream`
+ *   (a cudaStream_t; NULL = the legacy default stream).
+ * - Errors are returned BEFORE any launch and nothing is launched on error;
+ *   there is no fallback path.  A CUDA launch error maps to CP_ERR_CUDA.
+ * - Device pointers must be non-NULL and 16-byte aligned.
+ * - Layouts are token-major (rows of tokens, then heads, then head_dim):
+ *     Q        [b, S, h_q,  d]  bf16        K, V  [b, S, h_kv, d]  bf16
+ *     O        [b, S, h_q,  d]  fp32        m, l  [b, h_q, S]      fp32
+ *   Grouped-query heads map as kv_head = h / (h_q / h_kv).
+ * - The triple (m, l, O) of a query row over a key set J, x_j = scale*<q,k_j>:
+ *     m = max_j x_j (natural-log units), l = sum_j exp(x_j - m),
+ *     O = sum_j exp(x_j - m) v_j  (unnormalised).  The identity is (-inf, 0, 0).
+ *   ("Partial attention" row of the Terms table: max / numerator / denominator,
+ *   merged associatively and in any order.)
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CPATTN_API __attribute__((visibility("default")))
+#else
+#define CPATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARGUMENT = 1, /* bad size, pointer, alignment, step range, mode */
+  CP_ERR_UNSUPPORTED = 2,      /* valid request outside what the kernels implement (e.g. head_dim) */
+  CP_ERR_OVERFLOW = 3,         /* a byte count does not fit uint64 */
+  CP_ERR_CUDA = 4,             /* a CUDA runtime/driver call or launch failed */
+  CP_ERR_TIMEOUT = 5           /* a device-side wait gave up (reported by cp_take_device_status) */
+} cp_status;
+
+/* Modes of cp_ring_step_partial_attn.  FINALIZE may be OR-ed into either. */
+enum {
+  CP_MODE_EMIT = 0,       /* write the triple of the steps [step_begin, step_end) */
+  CP_MODE_ACCUMULATE = 1, /* merge that triple into the triple already in (o, m, l) */
+  CP_MODE_FINALIZE = 2    /* after that, write o = O / l (0 where l = 0); m, l stay */
+};
+
+/* Largest number of partial triples one cp_merge_partials call merges. */
+#define CP_MAX_MERGE_PARTS 256
+
+/* Static description of one attention problem (prefill or decode). */
+typedef struct {
+  int64_t b;      /* batch (sequences) */
+  int64_t S;      /* prefill: sequence length; decode: KV length L per sequence */
+  int64_t h_q;    /* query heads */
+  int64_t h_kv;   /* key/value heads, divides h_q */
+  int64_t d;      /* head dimension */
+  int64_t cp;     /* virtual ranks (prefill) or KV shards (decode); explicit, >= 1 */
+  float scale;    /* softmax scale, > 0 (the spec prints none; callers pass 1/sqrt(d)) */
+  int32_t causal; /* prefill: must be 1; decode: must be 0 */
+} cp_attn_desc;
+
+/* Human-readable name of a cp_status value (static storage, never NULL). */
+CPATTN_API const char* cp_status_string(int32_t status);
+
+/*
+ * Balanced head/tail chunk plan (Terms table, row "Balanced chunk split"; design
+ * rationale paragraph on balanced splitting; eq. g5cp-step-flops).
+ * The sequence is cut into 2*cp chunks of C = S/(2cp) tokens.  Rank r owns chunk
+ * r (head) and chunk 2cp-1-r (tail).  At ring step t rank r holds the K/V block of
+ * source rank (r - t) mod cp (step 0 = its own block; cp-1 rotations follow).
+ * Host-only; all arrays are caller-allocated host memory:
+ *   chunk_begin [2cp+1]  int64   first token of chunk k, chunk_begin[2cp] = S
+ *   rank_chunks [cp][2]  int32   {r, 2cp-1-r}
+ *   step_src    [cp][cp] int32   source rank of rank r at step t
+ *   step_pairs  [cp][cp] int64   visible (query,key) pairs per head of rank r at step t:
+ *                                2C^2, plus C at t = 0 (the two causal diagonals)
+ * Errors: cp < 1, S < 1, S % (2cp) != 0, or a NULL array -> CP_ERR_INVALID_ARGUMENT.
+ */
+CPATTN_API cp_status cp_plan_balanced_chunks(int64_t S, int32_t cp, int64_t* chunk_begin,
+                                  int32_t* rank_chunks, int32_t* step_src,
+                                  int64_t* step_pairs);
+
+/*
+ * Ring-step partial attention (Terms table rows "Pass-KV", "Ring step", "Partial
+ * attention"; eq. g5cp-step-flops) for ALL cp virtual ranks at once, over the ring
+ * steps [step_begin, step_end).  For every rank r, local query row i (global
+ * position) and step t, the visible keys are the rows of the two chunks of
+ * source rank s = (r - t) mod cp with key position <= i.  The steps are merged in
+ * ring order inside the kernel; the merged triple of each row is then
+ *   EMIT        written to (o, m, l) (rows that saw no key get the identity);
+ *   ACCUMULATE  merged into the triple already held in (o, m, l);
+ *   | FINALIZE  followed by o = O / l.
+ * EMIT | FINALIZE over [0, cp) is the complete causal attention in one launch.
+ * q, k, v: bf16 device, layouts above; o, m, l: fp32 device, layouts above.
+ * Supported: d in {64, 128}; causal = 1; every pointer 16-byte aligned.
+ * Errors: cp < 1, S % (2cp) != 0, h_q % h_kv != 0, any size < 1, scale <= 0 or
+ * not finite, 0 <= step_begin < step_end <= cp violated, unknown mode bits, NULL or
+ * misaligned pointer -> CP_ERR_INVALID_ARGUMENT; d outside {64,128} or causal != 1
+ * -> CP_ERR_UNSUPPORTED; a failed tensor-map encode or launch -> CP_ERR_CUDA.
+ */
+CPATTN_API cp_status cp_ring_step_partial_attn(const cp_attn_desc* desc, int32_t step_begin,
+                                    int32_t step_end, const void* q, const void* k,
+                                    const void* v, float* o, float* m, float* l,
+                                    int32_t mode, void* cuda_stream);
+
+/*
+ * LSE merge of n_parts partial triples (Terms table, row "Partial attention":
+ * the merge is associative and order-free; pass-Q paragraph of the
+ * Algorithm/formulas section: the reduce carries O, the max and the denominator).
+ *   o_parts [n_parts, batch, rows, heads, d]  m_parts, l_parts [n_parts, batch, heads, rows]
+ *   o_out   [batch, rows, heads, d]           m_out, l_out     [batch, heads, rows]
+ * (the prefill triple layout with rows = S; the decode partial layout with rows = 1).
+ * m = max_p m_p; l = sum_p e^{m_p - m} l_p; O = sum_p e^{m_p - m} O_p, the sums
+ * taken in the order given by `order` (a HOST array, a permutation of
+ * 0..n_parts-1; NULL = index order).  Parts with m_p = -inf weigh 0; a row whose
+ * parts are all the identity stays the identity.  finalize != 0 writes O / l
+ * (0 where l = 0) into o_out instead of O.  Outputs must not alias inputs.
+ * Errors: any size < 1, n_parts > CP_MAX_MERGE_PARTS, d % 4 != 0, `order` not a
+ * permutation, NULL or misaligned device pointer -> CP_ERR_INVALID_ARGUMENT;
+ * d > 512 -> CP_ERR_UNSUPPORTED.
+ */
+CPATTN_API cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t d,
+                            int32_t n_parts, const float* o_parts, const float* m_parts,
+                            const float* l_parts, const int32_t* order, float* o_out,
+                            float* m_out, float* l_out, int32_t finalize,
+                            void* cuda_stream);
+
+/*
+ * Bytes of device workspace cp_passq_decode needs for `desc` on the CURRENT
+ * device (the split count depends on its SM count).  Host-only.
+ * Errors: as cp_passq_decode's argument checks.
+ */
+CPATTN_API cp_status cp_passq_workspace_bytes(const cp_attn_desc* desc, size_t* bytes);
+
+/*
+ * Pass-Q decode (Terms table row "Pass-Q"; use-case decode paragraph; pass-Q
+ * paragraph of the Algorithm/formulas section).  One query per sequence is
+ * scored against cp KV shards: shard s holds keys [s*L/cp, (s+1)*L/cp) with
+ * L = desc->S; every key is visible.  Each shard is further split into equal
+ * key ranges so the whole GPU streams K/V; every range writes a partial triple to
+ * `workspace`, then the three-quantity reduce (the LSE merge, in shard order)
+ * writes
+ *   out   [b, h_q, d] fp32 = O / l,   m_out, l_out [b, h_q] fp32 (each nullable).
+ * q [b, h_q, d] bf16; k, v [b, L, h_kv, d] bf16.  The query dispatch of the spec
+ * is the shared q buffer.
+ * Supported: d in {64, 128, 256, 512}; h_q / h_kv in {1, 2, 4} with
+ * (h_q / h_kv) * d <= 1024; cp * splits <= CP_MAX_MERGE_PARTS; causal = 0.
+ * Errors: cp < 1, L % cp != 0, sizes < 1, h_q % h_kv != 0, scale <= 0, NULL or
+ * misaligned pointer, workspace_bytes below cp_passq_workspace_bytes ->
+ * CP_ERR_INVALID_ARGUMENT; unsupported d, group or causal -> CP_ERR_UNSUPPORTED.
+ */
+CPATTN_API cp_status cp_passq_decode(const cp_attn_desc* desc, const void* q, const void* k,
+                          const void* v, float* workspace, size_t workspace_bytes,
+                          float* out, float* m_out, float* l_out, void* cuda_stream);
+
+/* Inputs of the closed-form byte counts (all >= 0; cp >= 1). */
+typedef struct {
+  int64_t S;       /* sequence length */
+  int64_t cp;      /* CP degree */
+  int64_t c_kv;    /* K+V bytes per token per layer (both K and V already counted) */
+  int64_t b;       /* decode batch */
+  int64_t d;       /* model hidden size (length of the partial output vector) */
+  int64_t n_h;     /* attention heads */
+  int64_t s_dtype; /* bytes per element of the pass-Q messages */
+} cp_comm_query;
+
+typedef struct {
+  uint64_t passkv_total;    /* (cp-1) * (S/cp) * c_kv        eq. g5cp-passkv-bytes */
+  uint64_t passkv_per_step; /* (S/cp) * c_kv                 bytes of one ring step */
+  uint64_t passq_dispatch;  /* b * d * s_dtype               pass-Q query dispatch */
+  uint64_t passq_reduce;    /* b * (d + 2 n_h) * s_dtype     pass-Q reduce message */
+} cp_comm_result;
+
+/*
+ * Closed-form communication volumes (Algorithm/formulas section: eq.
+ * g5cp-passkv-bytes and the pass-Q paragraph), exact in uint64.  Host-only.
+ * The pass-KV formula carries no batch factor, as printed (per rank per layer).
+ * Errors: NULL pointer, a negative field, cp < 1, S % cp != 0 ->
+ * CP_ERR_INVALID_ARGUMENT; any result above 2^64-1 -> CP_ERR_OVERFLOW (the
+ * result struct is then left untouched).
+ */
+CPATTN_API cp_status cp_comm_bytes(const cp_comm_query* query, cp_comm_result* result);
+
+/*
+ * Synchronise `cuda_stream`, then read and clear the library's device status
+ * word on the current device.  Kernels never trap: a device-side wait that gives
+ * up records CP_ERR_TIMEOUT there and the kernel returns early (its outputs are
+ * then undefined).  *status receives CP_OK or the recorded error.
+ * Errors: NULL status -> CP_ERR_INVALID_ARGUMENT; a failed CUDA call -> CP_ERR_CUDA.
+ */
+CPATTN_API cp_status cp_take_device_status(void* cuda_stream, int32_t* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

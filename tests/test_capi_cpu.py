@@ -1,0 +1,202 @@
+"""C-ABI checks that need no GPU: symbols, host planner, byte counts, argument errors.
+
+No test here launches a kernel: every device-side call below carries an
+argument the library rejects before touching CUDA.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import comm as OC
+from oracle import ring as OR
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+
+@pytest.fixture(scope="module")
+def cpa():
+    from context_ring_attention_cp_gb300 import _build
+    _build.build()
+    import context_ring_attention_cp_gb300 as cpa
+    cpa.load_library()
+    return cpa
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CPATTN_API\s+[\w\s\*]+?\b(cp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for name in ["cp_plan_balanced_chunks", "cp_ring_step_partial_attn", "cp_merge_partials",
+                 "cp_passq_decode", "cp_comm_bytes", "cp_passq_workspace_bytes", "cp_status_string",
+                 "cp_take_device_status"]:
+        assert name in syms, name
+
+
+def test_library_exports_every_declared_symbol(cpa):
+    lib = ctypes.CDLL(cpa.library_path())
+    for name in _declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in cpattn.h but not exported"
+
+
+def test_status_strings(cpa):
+    assert cpa.cp_status_string(0) == "CP_OK"
+    assert cpa.cp_status_string(5) == "CP_ERR_TIMEOUT"
+    assert cpa.cp_status_string(99) == "CP_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("S,cp", [(2, 1), (8, 2), (24, 3), (64, 8), (96, 6), (1024, 2), (32768, 8),
+                                  (131072, 16), (1 << 20, 8), (4096, 32)])
+def test_plan_bit_exact_against_oracle(cpa, S, cp):
+    plan = cpa.cp_plan_balanced_chunks(S, cp)
+    assert plan["chunk_begin"].tolist() == OR.chunk_begin(S, cp)
+    assert plan["rank_chunks"].tolist() == OR.rank_chunks(cp)
+    assert plan["step_src"].tolist() == OR.step_source(cp)
+    assert plan["step_pairs"].tolist() == OR.step_pairs_closed_form(S, cp)
+    if S <= 128:
+        assert plan["step_pairs"].tolist() == OR.step_pairs_enumerated(S, cp)
+
+
+@pytest.mark.parametrize("S,cp", [(0, 1), (10, 0), (10, -2), (10, 3), (7, 1), (12, 4)])
+def test_plan_rejects(cpa, S, cp):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_plan_balanced_chunks(S, cp)
+    assert e.value.status == 1
+
+
+COMM_CASES = [
+    # (S, cp, c_kv, b, d, n_h, s)
+    (1024, 2, 2 * 4 * 64 * 2, 0, 0, 0, 0),
+    (32768, 8, 2 * 8 * 128 * 2, 0, 0, 0, 0),
+    (131072, 16, 2 * 8 * 128 * 2, 0, 0, 0, 0),
+    (131072, 8, 0, 8, 16 * 512, 16, 2),
+    (131072, 8, 0, 8, 16 * 512, 16, 4),
+    (1 << 20, 8, 320, 1, 7168, 128, 2),
+    (1 << 20, 1, 320, 1, 1, 1, 1),
+    (0, 4, 100, 0, 0, 0, 0),
+]
+
+
+@pytest.mark.parametrize("case", COMM_CASES)
+def test_comm_bytes_bit_exact_against_oracle(cpa, case):
+    S, cp, c_kv, b, d, n_h, s = case
+    got = cpa.cp_comm_bytes(S, cp, c_kv, b, d, n_h, s)
+    total, per = OC.passkv_bytes(S, cp, c_kv)
+    disp, red = OC.passq_bytes(b, d, n_h, s)
+    assert (got["passkv_total"], got["passkv_per_step"]) == (total, per)
+    assert (got["passq_dispatch"], got["passq_reduce"]) == (disp, red)
+
+
+def test_comm_bytes_at_the_workloads(cpa):
+    # c_kv for grouped-query attention: K and V, h_kv heads of d_head bf16 values
+    for S, cp, hkv, dh in [(1024, 2, 4, 64), (32768, 8, 8, 128), (131072, 16, 8, 128)]:
+        c_kv = OC.c_kv_gqa(hkv, dh, 2)
+        got = cpa.cp_comm_bytes(S, cp, c_kv)
+        assert got["passkv_total"] == OC.passkv_bytes(S, cp, c_kv)[0]
+
+
+def test_comm_bytes_overflow_and_errors(cpa):
+    big = (1 << 62)
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_comm_bytes(big, 2, 1 << 10)
+    assert e.value.status == 3
+    assert not OC.fits_u64(OC.passkv_bytes(big, 2, 1 << 10)[0])
+    # the largest values that still fit must come back exact
+    S = (1 << 63) - 2  # even, divisible by cp = 2
+    got = cpa.cp_comm_bytes(S, 2, 2)
+    assert got["passkv_per_step"] == OC.passkv_bytes(S, 2, 2)[1] <= OC.U64_MAX
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_comm_bytes(10, 3, 1)  # S not divisible by cp
+    assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_comm_bytes(10, 0, 1)
+    assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_comm_bytes(10, 1, 1, b=-1)
+    assert e.value.status == 1
+
+
+# --- device entry points: argument errors only (rejected before any CUDA call) ---
+
+FAKE = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced (rejected first)
+
+
+def _desc(cpa, **kw):
+    base = dict(b=1, S=1024, h_q=4, h_kv=4, d=64, cp=2, scale=0.125, causal=1)
+    base.update(kw)
+    return cpa.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cp=0), 1), (dict(cp=-1), 1), (dict(S=1000, cp=8), 1), (dict(S=0), 1), (dict(b=0), 1),
+    (dict(h_q=6, h_kv=4), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(causal=0), 2),
+])
+def test_ring_rejects_descriptors(cpa, kw, status):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_step_partial_attn(_desc(cpa, **kw), 0, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, stream=0)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("t0,t1,mode", [(-1, 1, 0), (1, 1, 0), (0, 3, 0), (2, 1, 0), (0, 2, 4), (0, 2, -1)])
+def test_ring_rejects_steps_and_modes(cpa, t0, t1, mode):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_step_partial_attn(_desc(cpa), t0, t1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, mode, stream=0)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("bad", [0, 1, 2, 3, 4, 5])
+def test_ring_rejects_null_or_misaligned(cpa, bad):
+    ptrs = [FAKE] * 6
+    for p in (0, FAKE + 8):
+        ptrs[bad] = p
+        with pytest.raises(cpa.CpError) as e:
+            cpa.cp_ring_step_partial_attn(_desc(cpa), 0, 2, *ptrs, 0, stream=0)
+        assert e.value.status == 1
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(batch=0), 1), (dict(rows=0), 1), (dict(n_parts=0), 1), (dict(n_parts=257), 1), (dict(d=6), 1),
+    (dict(d=516), 2), (dict(order=[0, 0]), 1), (dict(order=[0, 2]), 1), (dict(order=[1]), 1),
+    (dict(o_parts=FAKE + 4), 1), (dict(m_out=0), 1),
+])
+def test_merge_rejects(cpa, args, status):
+    kw = dict(batch=1, rows=8, heads=2, d=8, n_parts=2, o_parts=FAKE, m_parts=FAKE, l_parts=FAKE,
+              o_out=FAKE, m_out=FAKE, l_out=FAKE, order=None)
+    kw.update(args)
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_merge_partials(kw["batch"], kw["rows"], kw["heads"], kw["d"], kw["n_parts"], kw["o_parts"],
+                              kw["m_parts"], kw["l_parts"], kw["o_out"], kw["m_out"], kw["l_out"],
+                              order=kw["order"], stream=0)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(S=1000, cp=3), 1), (dict(cp=0), 1), (dict(d=96), 2), (dict(d=1024), 2), (dict(h_q=16, h_kv=2), 2),
+    (dict(h_q=8, h_kv=2, d=512), 2), (dict(causal=1), 2), (dict(h_q=3, h_kv=2), 1),
+])
+def test_decode_rejects(cpa, kw, status):
+    base = dict(b=2, S=1024, h_q=4, h_kv=4, d=128, cp=2, scale=0.1, causal=0)
+    base.update(kw)
+    desc = cpa.make_desc(**base)
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_passq_decode(desc, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE, stream=0)
+    assert e.value.status == status
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_passq_workspace_bytes(desc)
+    assert e.value.status == status
+
+
+def test_binding_has_no_fallback(tmp_path, monkeypatch):
+    import context_ring_attention_cp_gb300 as cpa
+    monkeypatch.setattr(cpa, "_LIB", None)
+    monkeypatch.setattr(cpa, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        cpa.cp_comm_bytes(8, 2, 1)

@@ -1,0 +1,193 @@
+"""LSE merge and pass-Q decode on the GPU against the fp64 oracle (parity tests).
+
+Merge tolerance: per row, max|gpu - ref| / max|ref| <= 1e-5, for the oracle and
+between any two merge orders; m is exact (max is order-free).  Decode: output
+max-abs <= 2e-2, mean-abs <= 2e-3, lse within 2e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import context_ring_attention_cp_gb300 as cpa
+from context_ring_attention_cp_gb300 import synth
+from oracle import attention as OA
+from oracle import ring as OR
+
+from gpu_util import LSE_ABS, MERGE_REL, assert_out_close, assert_rowwise_rel, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from context_ring_attention_cp_gb300 import _build
+    _build.build()
+    cpa.load_library()
+
+
+def _merge(o, m, l, order=None, finalize=False):
+    n, b, rows, heads, d = o.shape
+    oo = torch.empty((b, rows, heads, d), dtype=torch.float32, device=o.device)
+    mo = torch.empty((b, heads, rows), dtype=torch.float32, device=o.device)
+    lo = torch.empty_like(mo)
+    cpa.cp_merge_partials(b, rows, heads, d, n, o, m, l, oo, mo, lo, order=order, finalize=finalize)
+    return oo, mo, lo
+
+
+def _oracle_parts(o, m, l, heads_sel):
+    """Oracle-layout triples [rows*heads_sel] for each part (fp64)."""
+    parts = []
+    for p in range(o.shape[0]):
+        om = o[p, 0][:, heads_sel].cpu().double().numpy()          # [rows, H, d]
+        mm = m[p, 0][heads_sel].cpu().double().numpy().T            # [rows, H]
+        ll = l[p, 0][heads_sel].cpu().double().numpy().T
+        parts.append((mm, ll, om))
+    return parts
+
+
+@pytest.mark.parametrize("shape", [(4, 1, 37, 3, 8), (32, 1, 96, 5, 128), (7, 2, 33, 2, 64), (3, 1, 5, 2, 512),
+                                   (256, 1, 32, 1, 16), (1, 1, 70, 4, 128)])
+def test_merge_matches_oracle_small(shape):
+    n, b, rows, heads, d = shape
+    draws = [synth.merge_parts(n, heads, rows, d, spread=80.0, seed=n * 31 + d + bi) for bi in range(b)]
+    o = torch.cat([x[0] for x in draws], dim=1).contiguous()  # [n, b, rows, heads, d]
+    m = torch.cat([x[1] for x in draws], dim=1).contiguous()  # [n, b, heads, rows]
+    l = torch.cat([x[2] for x in draws], dim=1).contiguous()
+    rng = np.random.default_rng(n)
+    order = rng.permutation(n)
+    for fin in (False, True):
+        go, gm, gl = _merge(o, m, l, order=order, finalize=fin)
+        torch.cuda.synchronize()
+        for bi in range(b):
+            parts = [(m[p, bi].T.cpu().double().numpy(), l[p, bi].T.cpu().double().numpy(),
+                      o[p, bi].cpu().double().numpy()) for p in range(n)]
+            rm, rl, ro = OR.merge_in_order(parts, order)
+            assert np.array_equal(gm[bi].T.cpu().double().numpy(), rm)
+            assert np.abs(gl[bi].T.cpu().double().numpy() - rl).max() <= MERGE_REL * max(1.0, np.abs(rl).max())
+            if fin:
+                ref, _ = OR.finalize((rm, rl, ro))
+            else:
+                ref = ro
+            assert_rowwise_rel(go[bi].cpu().numpy(), ref, MERGE_REL, f"merge {shape} fin={fin}")
+
+
+def test_merge_identity_rows_and_single_part():
+    n, rows, heads, d = 3, 40, 2, 32
+    o, m, l = synth.merge_parts(n, heads, rows, d, seed=4)
+    m[:, :, :, 7] = -math.inf; l[:, :, :, 7] = 0; o[:, :, 7] = 0  # a row that is the identity everywhere
+    go, gm, gl = _merge(o, m, l, finalize=True)
+    torch.cuda.synchronize()
+    assert torch.isneginf(gm[0, :, 7]).all() and (gl[0, :, 7] == 0).all() and (go[0, 7] == 0).all()
+    assert not torch.isnan(go).any()
+    # one part is returned as is (m, l exact; O exact when not finalised)
+    go1, gm1, gl1 = _merge(o[:1], m[:1], l[:1])
+    torch.cuda.synchronize()
+    assert torch.equal(gm1, m[0]) and torch.equal(gl1, l[0]) and torch.equal(go1, o[0])
+
+
+def test_merge_stress_workload_orders_and_tree():
+    """64 heads x 128 x 4096 rows, 32 parts, spread +-80: 10 seeded orders and one tree order."""
+    w = synth.WORKLOADS["merge"]
+    n, heads, rows, d = w["parts"], w["heads"], w["rows"], w["d"]
+    o, m, l = synth.merge_parts(n, heads, rows, d, spread=w["spread"], seed=w["seed"])
+    rng = np.random.default_rng(w["seed"])
+    orders = [rng.permutation(n) for _ in range(10)]
+    outs = []
+    for order in orders:
+        go, gm, gl = _merge(o, m, l, order=order)
+        outs.append((go, gm, gl))
+    torch.cuda.synchronize()
+    # tree order: balanced pairwise merges over index order with n_parts = 2 calls
+    level = [(o[p:p + 1], m[p:p + 1], l[p:p + 1]) for p in range(n)]
+    while len(level) > 1:
+        nxt = []
+        for i in range(0, len(level), 2):
+            a, b = level[i], level[i + 1]
+            co, cm, cl = _merge(torch.cat([a[0], b[0]]), torch.cat([a[1], b[1]]), torch.cat([a[2], b[2]]))
+            nxt.append((co.unsqueeze(0), cm.unsqueeze(0), cl.unsqueeze(0)))
+        level = nxt
+    tree = (level[0][0][0], level[0][1][0], level[0][2][0])
+    torch.cuda.synchronize()
+    ref_o, ref_m, ref_l = outs[0]
+    for go, gm, gl in outs[1:] + [tree]:
+        assert torch.equal(gm, ref_m)  # max is exact in any order
+        assert ((gl - ref_l).abs() <= MERGE_REL * ref_l.abs()).all()
+        err = (go - ref_o).abs().amax(dim=-1)
+        scale = ref_o.abs().amax(dim=-1)
+        assert (err <= MERGE_REL * scale).all()
+    # oracle on a head subset (fp64 over all 32 parts, fold in the first order)
+    hs = [0, 17, 63]
+    parts = _oracle_parts(o, m, l, hs)
+    rm, rl, ro = OR.merge_in_order(parts, orders[0])
+    assert np.array_equal(ref_m[0][hs].T.cpu().double().numpy(), rm)
+    assert_rowwise_rel(ref_o[0][:, hs].cpu().numpy(), ro, MERGE_REL, "merge stress vs oracle")
+    assert np.abs(ref_l[0][hs].T.cpu().double().numpy() - rl).max() <= MERGE_REL * np.abs(rl).max()
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode(q, k, v, cp):
+    b, hq, d = q.shape
+    L, hkv = k.shape[1], k.shape[2]
+    desc = cpa.make_desc(b, L, hq, hkv, d, cp, 1.0 / math.sqrt(d), 0)
+    ws_bytes = cpa.cp_passq_workspace_bytes(desc)
+    ws = torch.empty(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    mo = torch.empty((b, hq), dtype=torch.float32, device="cuda")
+    lo = torch.empty_like(mo)
+    cpa.cp_passq_decode(desc, q, k, v, ws, ws_bytes, out, mo, lo)
+    assert cpa.cp_take_device_status() == 0
+    return out, mo, lo
+
+
+DECODE_SMALL = [(2, 4096, 4, 4, 128, 4), (3, 2048, 8, 2, 64, 2), (1, 1024, 2, 1, 256, 1),
+                (2, 8192, 16, 16, 512, 8), (1, 3000, 4, 2, 512, 3), (2, 96, 4, 4, 128, 8),
+                (1, 12, 2, 2, 64, 4)]
+
+
+@pytest.mark.parametrize("case", DECODE_SMALL, ids=[str(c) for c in DECODE_SMALL])
+def test_decode_matches_oracle(case):
+    b, L, hq, hkv, d, cp = case
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=L + d)
+    out, mo, lo = _decode(q, k, v, cp)
+    ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(out.cpu().numpy(), ref_out, f"decode {case}")
+    lse = (mo + torch.log(lo)).cpu().numpy()
+    assert np.abs(lse - (ref_m + np.log(ref_l))).max() <= LSE_ABS
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+def test_decode_shards_do_not_change_the_answer():
+    b, L, hq, hkv, d = 2, 4096, 4, 4, 128
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=3)
+    base = _decode(q, k, v, 1)[0]
+    for cp in (2, 4, 8, 16):
+        assert (_decode(q, k, v, cp)[0] - base).abs().max().item() <= 1e-4
+
+
+def test_decode_workload_sampled_heads():
+    """b8, 16 heads, d512, L131072, cp8 at full size; oracle on sampled (sequence, head) pairs."""
+    w = synth.WORKLOADS["decode"]
+    q, k, v = synth.decode_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], seed=w["seed"])
+    out, mo, lo = _decode(q, k, v, w["cp"])
+    scale = 1.0 / math.sqrt(w["d"])
+    for bi, h in [(0, 0), (3, 7), (7, 15), (5, 2)]:
+        ref_out, ref_m, ref_l = OA.decode_attention(f64(q[bi:bi + 1, h:h + 1]), f64(k[bi:bi + 1, :, h:h + 1]),
+                                                    f64(v[bi:bi + 1, :, h:h + 1]), scale)
+        assert_out_close(out[bi, h].cpu().numpy(), ref_out[0, 0], f"decode workload ({bi},{h})")
+        assert abs(float(mo[bi, h] + torch.log(lo[bi, h])) - float(ref_m[0, 0] + np.log(ref_l[0, 0]))) <= LSE_ABS
+    del q, k, v
+    torch.cuda.empty_cache()
+
+
+def test_decode_rejects_small_workspace():
+    q, k, v = synth.decode_inputs(1, 256, 2, 2, 128, seed=1)
+    desc = cpa.make_desc(1, 256, 2, 2, 128, 2, 0.1, 0)
+    need = cpa.cp_passq_workspace_bytes(desc)
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    out = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(cpa.CpError):
+        cpa.cp_passq_decode(desc, q, k, v, ws, need - 4, out)

@@ -1,0 +1,180 @@
+"""Ring-step prefill attention on the GPU against the fp64 oracle (parity tests).
+
+Tolerances (bf16 inputs, fp32 accumulation): output max-abs <= 2e-2 and
+mean-abs <= 2e-3; per-step lse = m + ln l within 2e-3; rows that see no key in
+a step must be exactly the identity (-inf, 0, 0).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import context_ring_attention_cp_gb300 as cpa
+from context_ring_attention_cp_gb300 import synth
+from oracle import attention as OA
+from oracle import ring as OR
+
+from gpu_util import (LSE_ABS, assert_out_close, f64, ring_buffers, run_ring)
+
+pytestmark = pytest.mark.gpu
+
+EMIT, ACC, FIN = cpa.CP_MODE_EMIT, cpa.CP_MODE_ACCUMULATE, cpa.CP_MODE_FINALIZE
+
+# (b, S, h_q, h_kv, d, cp, std): several 128-row tiles, ragged chunk tails (C % 128 != 0),
+# odd and even GQA groups, cp = 1, a single-token chunk, batch > 1.
+SMALL = [
+    (1, 1024, 4, 4, 64, 2, 1.0),     # the tiny workload
+    (2, 512, 4, 2, 128, 2, 0.5),
+    (1, 1000, 2, 1, 128, 2, 1.0),    # C = 250: 128 + 122-row tiles
+    (1, 768, 6, 2, 64, 4, 1.0),      # C = 96 < 128, g = 3 (a pair and a single)
+    (1, 2048, 8, 2, 128, 8, 0.5),    # C = 128
+    (1, 384, 3, 3, 64, 1, 1.0),      # cp = 1
+    (1, 8, 2, 2, 64, 4, 1.0),        # C = 1
+    (3, 640, 4, 1, 128, 5, 0.5),     # C = 64, g = 4, b = 3
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from context_ring_attention_cp_gb300 import _build
+    _build.build()
+    cpa.load_library()
+
+
+def _inputs(b, S, hq, hkv, d, std, seed):
+    return synth.prefill_inputs(b, S, hq, hkv, d, std=std, seed=seed, device="cuda")
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[str(c) for c in SMALL])
+def test_full_ring_equals_causal_attention(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=hash(case) & 0xFFFF)
+    o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    ref_out, ref_m, ref_l, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(o.cpu().numpy(), ref_out, f"out {case}")
+    lse = (m + torch.log(l)).cpu().numpy()
+    assert np.abs(lse - (ref_m + np.log(ref_l))).max() <= LSE_ABS
+    assert np.abs(m.cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("case", SMALL[:6], ids=[str(c) for c in SMALL[:6]])
+def test_each_step_emits_the_oracle_step_triple(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=7 + (hash(case) & 0xFF))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    scale = 1.0 / math.sqrt(d)
+    for t in range(cp):
+        o, m, l = run_ring(q, k, v, cp, t, t + 1, EMIT)
+        o, m, l = o.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy()
+        for r in range(cp):
+            rows, rm, rl, ro = OR.ring_step_triple(qf, kf, vf, scale, cp, r, t)
+            gm, gl = m[:, :, rows], l[:, :, rows]
+            go = np.moveaxis(o[:, rows], 1, 2)  # [b, hq, rows, d]
+            empty = np.isneginf(rm)
+            assert np.all(np.isneginf(gm[empty])) and np.all(gl[empty] == 0) and np.all(go[empty] == 0)
+            live = ~empty
+            assert np.all(np.isfinite(gm[live])) and np.all(gl[live] > 0)
+            assert np.abs((gm + np.log(np.where(live, gl, 1)))[live] - (rm + np.log(np.where(live, rl, 1)))[live]).max() <= LSE_ABS
+            assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
+            ref_out = ro[live] / rl[live][:, None]
+            assert_out_close(go[live] / gl[live][:, None], ref_out, f"step {t} rank {r}")
+
+
+@pytest.mark.parametrize("case", [SMALL[1], SMALL[3], SMALL[7]], ids=["b2", "ragged_g3", "cp5"])
+def test_accumulate_steps_then_finalize(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=99)
+    bufs = ring_buffers(b, S, hq, d, identity=True)
+    order = list(range(cp))[::-1]  # any step order merges to the same result
+    for i, t in enumerate(order):
+        mode = ACC | (FIN if i == cp - 1 else 0)
+        run_ring(q, k, v, cp, t, t + 1, mode, bufs)
+    ref_out, ref_m, ref_l, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(bufs[0].cpu().numpy(), ref_out, "accumulated")
+    assert np.abs(bufs[1].cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+def test_emit_then_merge_kernel_finalize_matches_fused():
+    b, S, hq, hkv, d, cp = 1, 1024, 4, 2, 128, 4
+    q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=5)
+    fo, fm, fl = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    eo, em, el = run_ring(q, k, v, cp, 0, cp, EMIT)
+    out = torch.empty_like(eo); mo = torch.empty_like(em); lo = torch.empty_like(el)
+    cpa.cp_merge_partials(b, S, hq, d, 1, eo, em, el, out, mo, lo, finalize=True)
+    torch.cuda.synchronize()
+    assert torch.equal(mo, fm) and torch.equal(lo, fl)
+    assert (out - fo).abs().max().item() <= 1e-6
+
+
+def test_two_step_ranges_accumulate_to_full():
+    b, S, hq, hkv, d, cp = 1, 2048, 4, 4, 64, 8
+    q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=6)
+    bufs = ring_buffers(b, S, hq, d, identity=True)
+    run_ring(q, k, v, cp, 0, 3, ACC, bufs)
+    run_ring(q, k, v, cp, 3, cp, ACC | FIN, bufs)
+    ref = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    assert (bufs[0] - ref[0]).abs().max().item() <= 1e-4
+    ref_out, _, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(bufs[0].cpu().numpy(), ref_out, "two ranges")
+
+
+def test_cp1_equals_unsplit_and_any_cp_agrees():
+    b, S, hq, hkv, d = 1, 1536, 4, 2, 128
+    q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=8)
+    base = run_ring(q, k, v, 1, 0, 1, EMIT | FIN)[0]
+    for cp in (2, 3, 4, 6):
+        other = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)[0]
+        assert (other - base).abs().max().item() <= 2e-3, cp
+
+
+def test_extreme_logits_stay_finite():
+    # large logits force exponent-reference raises and O rescaling inside the kernel
+    b, S, hq, hkv, d, cp = 1, 1024, 2, 2, 128, 2
+    q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=9)
+    ramp = torch.linspace(0.0, 6.0, S, device="cuda").view(1, S, 1, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    q = (q.float() * 3.0).to(torch.bfloat16)
+    o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    ref_out, ref_m, ref_l, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(o.cpu().numpy(), ref_out, "extreme")
+    assert np.abs((m + torch.log(l)).cpu().numpy() - (ref_m + np.log(ref_l))).max() <= LSE_ABS * 10
+
+
+def test_invalid_arguments_launch_nothing():
+    q, k, v = _inputs(1, 256, 2, 2, 64, 1.0, seed=1)
+    o, m, l = ring_buffers(1, 256, 2, 64)
+    desc = cpa.make_desc(1, 256, 2, 2, 64, 3, 0.125, 1)  # 256 % 6 != 0
+    with pytest.raises(cpa.CpError):
+        cpa.cp_ring_step_partial_attn(desc, 0, 3, q, k, v, o, m, l, EMIT)
+    desc = cpa.make_desc(1, 256, 2, 2, 64, 2, 0.125, 1)
+    with pytest.raises(cpa.CpError):
+        cpa.cp_ring_step_partial_attn(desc, 0, 2, q, k, v, o[:, :, :, 1:], m, l, EMIT)  # misaligned
+    assert cpa.cp_take_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["gqa", "long"])
+def test_full_size_workload_sampled_rows(name):
+    """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled."""
+    w = synth.WORKLOADS[name]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o, m, l = run_ring(q, k, v, w["cp"], 0, w["cp"], EMIT | FIN)
+    rows = synth.sample_rows(w["S"], w["cp"], 64, seed=w["seed"])
+    heads = [0, 5, w["h_q"] - 1]
+    g = w["h_q"] // w["h_kv"]
+    scale = 1.0 / math.sqrt(w["d"])
+    for h in heads:
+        kh = h // g
+        qs = f64(q[0, rows, h:h + 1])                          # [R, 1, d]
+        ks = f64(k[0, :, kh:kh + 1])[None]                    # [1, S, 1, d]
+        vs = f64(v[0, :, kh:kh + 1])[None]
+        qfull = np.zeros((1, w["S"], 1, w["d"]))
+        qfull[0, rows] = qs
+        ref_out, ref_m, ref_l = OA.causal_attention_rows(qfull, ks, vs, scale, 0, [0], rows)
+        got = o[0, rows, h].cpu().numpy()
+        assert_out_close(got, ref_out[0], f"{name} head {h}")
+        lse = (m[0, h, rows] + torch.log(l[0, h, rows])).cpu().numpy()
+        assert np.abs(lse - (ref_m[0] + np.log(ref_l[0]))).max() <= LSE_ABS
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
