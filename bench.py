@@ -1,0 +1,461 @@
+"""Benchmark of the ring-step prefill (and pass-Q decode / merge) on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass of the hot path over the GQA prefill workload (b1,
+32 q / 8 kv heads, d128, S32768, cp8): the host chunk plan, the ring-step
+attention of all cp virtual ranks over all cp steps in one launch (the
+between-step merge fused, output finalised), and the closed-form byte counts.
+Inputs (402 MB of bf16 Q/K/V) exceed the 129 MB L2, so no flush is needed.
+
+Rank 0 prints one JSON line.  ``value`` is prefill TFLOP/s over all ranks
+(algorithmic FLOPs 4*b*h_q*d*S(S+1)/2 per step).  Under torchrun every rank runs
+an independent replica (weak scaling, no collective on the data path).
+The line also carries the dominant kernel's roofline, an end-to-end number
+through the C-ABI with host buffers, the CPU oracle baseline, SM clocks sampled
+during the timed region, and secondary lines for pass-Q decode (GB/s) and the
+LSE merge (GB/s).
+
+``--impl reference`` times the CPU oracle (fp64, test infrastructure) on a
+bounded row sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import os
+
+if os.environ.get("CPATTN_ORACLE_WORKER") == "1":
+    # spawned oracle workers: one BLAS thread each, so `cores` is the pool size
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+WORKLOAD = "gqa"
+METRIC = "ring-step prefill TFLOP/s (% bf16 peak); pass-Q decode GB/s (% HBM peak)"
+
+
+# ---------------------------------------------------------------------------
+# workload arithmetic (algorithmic work, not what the kernels happen to move)
+# ---------------------------------------------------------------------------
+
+def prefill_flops(w):
+    pairs = w["S"] * (w["S"] + 1) // 2
+    return 4 * w["b"] * w["h_q"] * w["d"] * pairs
+
+
+def decode_bytes(w):
+    b, L, hq, hkv, d, cp = w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"]
+    kv = 2 * b * L * hkv * d * 2
+    q = b * hq * d * 2
+    partials = 2 * cp * b * hq * (d + 2) * 4  # written once, read once by the reduce
+    out = b * hq * d * 4
+    return kv + q + partials + out
+
+
+def merge_bytes(w):
+    n, h, r, d = w["parts"], w["heads"], w["rows"], w["d"]
+    return n * h * r * (d + 2) * 4 + h * r * (d + 2) * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip() for r in self.file.read().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (test infrastructure) on a bounded row sample
+# ---------------------------------------------------------------------------
+
+def _oracle_rows_task(args):
+    """One worker: causal attention for sampled rows of one head (fp64 oracle)."""
+    qbits, kbits, vbits, rows, scale = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from oracle import attention as OA
+    q = oracle.bf16_bits_to_f64(qbits)   # [R, d] rows of this head
+    k = oracle.bf16_bits_to_f64(kbits)   # [S, d] of its kv head
+    v = oracle.bf16_bits_to_f64(vbits)
+    S, d = k.shape
+    t0 = time.perf_counter()
+    qfull = np.zeros((1, S, 1, d))
+    qfull[0, rows, 0] = q
+    OA.causal_attention_rows(qfull, k[None, :, None], v[None, :, None], scale, 0, [0], rows)
+    dt = time.perf_counter() - t0
+    flops = sum(4 * d * (i + 1) for i in rows)
+    return flops, dt
+
+
+def oracle_sample_tasks(w, q, k, v, rows_per_head, heads, seed):
+    from context_ring_attention_cp_gb300 import synth
+    rng = np.random.default_rng(seed)
+    g = w["h_q"] // w["h_kv"]
+    tasks = []
+    for h in heads:
+        rows = sorted(int(x) for x in rng.integers(0, w["S"], size=rows_per_head))
+        kh = h // g
+        tasks.append((synth.bf16_bits(q[0, rows, h]), synth.bf16_bits(k[0, :, kh]), synth.bf16_bits(v[0, :, kh]),
+                      rows, 1.0 / math.sqrt(w["d"])))
+    return tasks
+
+
+def run_oracle_pool(tasks, workers):
+    """Times the oracle over ``tasks`` on a spawn pool of single-threaded workers."""
+    import multiprocessing as mp
+    os.environ["CPATTN_ORACLE_WORKER"] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers) as pool:
+            pool.map(_oracle_rows_task, tasks[:workers])  # warm the workers (imports)
+            t0 = time.perf_counter()
+            res = pool.map(_oracle_rows_task, tasks)
+            wall = time.perf_counter() - t0
+    finally:
+        os.environ.pop("CPATTN_ORACLE_WORKER", None)
+    flops = sum(r[0] for r in res)
+    return flops, wall
+
+
+# ---------------------------------------------------------------------------
+# GPU arms
+# ---------------------------------------------------------------------------
+
+def _events_time(fn, iters, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(iters):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / iters
+
+
+def bench_ours(args, rank, world, dist):
+    import torch
+
+    import context_ring_attention_cp_gb300 as cpa
+    from context_ring_attention_cp_gb300 import _build, synth
+
+    if rank == 0 or world == 1:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    cpa.load_library()
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    w = synth.WORKLOADS[WORKLOAD]
+    b, S, hq, hkv, d, cp = w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"]
+    q, k, v = synth.prefill_inputs(b, S, hq, hkv, d, std=w["std"], seed=w["seed"] + rank)
+    o = torch.empty((b, S, hq, d), dtype=torch.float32, device="cuda")
+    m = torch.empty((b, hq, S), dtype=torch.float32, device="cuda")
+    l = torch.empty((b, hq, S), dtype=torch.float32, device="cuda")
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+    mode = cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE
+    c_kv = 2 * hkv * d * 2
+    flops = prefill_flops(w)
+    kernel_ms = []
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+
+    def step(i=None):
+        plan = cpa.cp_plan_balanced_chunks(S, cp)              # a1: chunk plan (host)
+        if i is not None:
+            ev[2 * i].record(stream)
+        cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, o, m, l, mode, stream)  # a2-a4 (one launch)
+        if i is not None:
+            ev[2 * i + 1].record(stream)
+        cpa.cp_comm_bytes(S, cp, c_kv)                         # a6: byte accounting (host)
+        return plan
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if cpa.cp_take_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    sampler = ClockSampler(dev)
+    sampler.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    kernel_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    if cpa.cp_take_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    kern_ms = statistics.mean(kernel_ms)
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "ring_attn_kernel<128>", "kernel_ms": round(kern_ms, 4),
+                "peak_kind": f"bf16 sustained ({peaks['source']})",
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
+
+    # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.skip_e2e:
+        hq_, hk_, hv_ = (x.cpu().pin_memory() for x in (q, k, v))
+        ho = torch.empty(o.shape, dtype=torch.float32).pin_memory()
+        hm = torch.empty(m.shape, dtype=torch.float32).pin_memory()
+        hl = torch.empty(l.shape, dtype=torch.float32).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq_, non_blocking=True)
+            dk.copy_(hk_, non_blocking=True)
+            dv.copy_(hv_, non_blocking=True)
+            cpa.cp_plan_balanced_chunks(S, cp)
+            cpa.cp_ring_step_partial_attn(desc, 0, cp, dq, dk, dv, o, m, l, mode, stream)
+            ho.copy_(o, non_blocking=True)
+            hm.copy_(m, non_blocking=True)
+            hl.copy_(l, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 3),
+               "h2d_bytes_per_step": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2),
+               "d2h_bytes_per_step": int((o.numel() + m.numel() + l.numel()) * 4)}
+        del hq_, hk_, hv_, ho, hm, hl, dq, dk, dv
+
+    secondary = {}
+    if not args.skip_secondary and rank == 0:
+        secondary = secondary_lines(cpa, synth, peaks, stream)
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        tasks = oracle_sample_tasks(w, q, k, v, args.cpu_rows, list(range(0, hq, max(1, hq // args.cpu_workers)))[
+            :args.cpu_workers], seed=w["seed"])
+        cpu_flops, cpu_s = run_oracle_pool(tasks, args.cpu_workers)
+        cpu = {"value": round(cpu_flops / cpu_s / 1e12, 6), "unit": "TFLOP/s", "cores": args.cpu_workers,
+               "kind": "oracle",
+               "sample": f"{len(tasks)} heads x {args.cpu_rows} random rows of the {WORKLOAD} workload "
+                         f"(causal rows, fp64 numpy), {cpu_s:.1f} s on a spawn pool of {args.cpu_workers} "
+                         "single-threaded workers"}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V)",
+            "config": {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
+                       "b": b, "S": S, "h_q": hq, "h_kv": hkv, "d": d, "cp": cp,
+                       "step": "plan + one ring launch over all cp steps (merge fused, finalised) + byte counts",
+                       "l2": "inputs (402 MB) larger than L2; no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clocks, "secondary": secondary}
+    return line
+
+
+def secondary_lines(cpa, synth, peaks, stream):
+    import torch
+    out = {}
+    # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)
+    w = synth.WORKLOADS["decode"]
+    q, k, v = synth.decode_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], seed=w["seed"])
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 0)
+    nbytes = cpa.cp_passq_workspace_bytes(desc)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    res = torch.empty((w["b"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    fn = lambda: cpa.cp_passq_decode(desc, q, k, v, ws, nbytes, res, None, None, stream)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 10, stream)
+    gbs = decode_bytes(w) / (ms * 1e-3) / 1e9
+    out["decode"] = {"workload": "pass-Q decode: b8, 16 heads, d512, L131072, cp8", "value": round(gbs, 1),
+                     "unit": "GB/s", "ms": round(ms, 4), "bytes": decode_bytes(w), "peak": peaks["hbm_gbs"],
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": 2}
+    del q, k, v, ws
+    torch.cuda.empty_cache()
+    # LSE merge: 32 parts x 64 heads x 4096 rows x 128
+    w = synth.WORKLOADS["merge"]
+    po, pm, pl = synth.merge_parts(w["parts"], w["heads"], w["rows"], w["d"], spread=w["spread"], seed=w["seed"])
+    mo = torch.empty((1, w["rows"], w["heads"], w["d"]), dtype=torch.float32, device="cuda")
+    mm = torch.empty((1, w["heads"], w["rows"]), dtype=torch.float32, device="cuda")
+    ml = torch.empty_like(mm)
+    order = np.random.default_rng(w["seed"]).permutation(w["parts"])
+    fn = lambda: cpa.cp_merge_partials(1, w["rows"], w["heads"], w["d"], w["parts"], po, pm, pl, mo, mm, ml,  # noqa
+                                       order=order, stream=stream)
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 20, stream)
+    gbs = merge_bytes(w) / (ms * 1e-3) / 1e9
+    out["merge"] = {"workload": "LSE merge: 32 parts x 64 heads x 4096 rows x 128", "value": round(gbs, 1),
+                    "unit": "GB/s", "ms": round(ms, 4), "bytes": merge_bytes(w), "peak": peaks["hbm_gbs"],
+                    "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    del po, pm, pl, mo
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_reference(args, rank, world):
+    """The CPU oracle as the reference arm: bounded row samples of the same workload."""
+    if rank != 0:
+        return None
+    import torch
+    from context_ring_attention_cp_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"],
+                                   device="cpu")
+    heads = list(range(0, w["h_q"], max(1, w["h_q"] // args.cpu_workers)))[:args.cpu_workers]
+    rows = max(4, args.cpu_rows // 8)
+    for i in range(args.warmup):
+        run_oracle_pool(oracle_sample_tasks(w, q, k, v, rows, heads, seed=i), args.cpu_workers)
+    tot_flops, tot_s = 0, 0.0
+    for i in range(args.steps):
+        f, s = run_oracle_pool(oracle_sample_tasks(w, q, k, v, rows, heads, seed=1000 + i), args.cpu_workers)
+        tot_flops += f
+        tot_s += s
+    value = tot_flops / tot_s / 1e12
+    sample = (f"per step {len(heads)} heads x {rows} random rows (causal, fp64 numpy oracle) on a spawn pool of "
+              f"{args.cpu_workers} single-threaded workers")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V)",
+            "config": {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
+                       "b": w["b"], "S": w["S"], "h_q": w["h_q"], "h_kv": w["h_kv"], "d": w["d"], "cp": w["cp"]},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": args.cpu_workers,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-workers", type=int, default=min(16, os.cpu_count() or 1))
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-secondary", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    sys.path.insert(0, ROOT)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as tdist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line = bench_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -115,7 +115,10 @@ def test_two_step_ranges_accumulate_to_full():
     run_ring(q, k, v, cp, 0, 3, ACC, bufs)
     run_ring(q, k, v, cp, 3, cp, ACC | FIN, bufs)
     ref = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
-    assert (bufs[0] - ref[0]).abs().max().item() <= 1e-4
+    # P is rounded to bf16 against each launch's own exponent reference, so two
+    # launches and one fused launch differ at that rounding level (both are
+    # checked against the oracle below).
+    assert (bufs[0] - ref[0]).abs().max().item() <= 5e-3
     ref_out, _, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
     assert_out_close(bufs[0].cpu().numpy(), ref_out, "two ranges")
 
