@@ -172,6 +172,12 @@ def oracle_sample_tasks(w, q, k, v, rows_per_head, heads, seed):
     return tasks
 
 
+def _oracle_warm(_):
+    sys.path.insert(0, ROOT)
+    import oracle  # noqa: F401
+    return 0
+
+
 def run_oracle_pool(tasks, workers):
     """Times the oracle over ``tasks`` on a spawn pool of single-threaded workers."""
     import multiprocessing as mp
@@ -179,7 +185,7 @@ def run_oracle_pool(tasks, workers):
     try:
         ctx = mp.get_context("spawn")
         with ctx.Pool(workers) as pool:
-            pool.map(_oracle_rows_task, tasks[:workers])  # warm the workers (imports)
+            pool.map(_oracle_warm, range(workers))  # imports happen outside the timed map
             t0 = time.perf_counter()
             res = pool.map(_oracle_rows_task, tasks)
             wall = time.perf_counter() - t0
