@@ -68,6 +68,21 @@ def merge_bytes(w):
     return n * h * r * (d + 2) * 4 + h * r * (d + 2) * 4
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# ring kernel on this workload, from the ncu capture summarised in
+# profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
+# the source that was captured (sha256 prefix below); otherwise traffic is null.
+RING_TRAFFIC = {"sha256_prefix": "c93a0a01dcc05625", "bytes": 2258198728}
+
+
+def ring_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "context_ring_attention_cp_gb300", "csrc", "ring_attn.cu")
+    with open(path, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return RING_TRAFFIC["bytes"] if digest.startswith(RING_TRAFFIC["sha256_prefix"]) else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -283,7 +298,8 @@ def bench_ours(args, rank, world, dist):
     achieved = flops / (kern_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": ring_traffic(),
+                "algorithmic_bytes": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + (o.numel() + 2 * m.numel()) * 4),
                 "kernel": "ring_attn_kernel<128>", "kernel_ms": round(kern_ms, 4),
                 "peak_kind": f"bf16 sustained ({peaks['source']})",
                 "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
@@ -431,7 +447,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-workers", type=int, default=min(16, os.cpu_count() or 1))
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=1536)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
