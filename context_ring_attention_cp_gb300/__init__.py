@@ -22,7 +22,7 @@ __all__ = [
     "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE",
     "CP_MAX_MERGE_PARTS", "library_path", "load_library", "cp_status_string",
     "cp_plan_balanced_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn", "cp_merge_partials",
-    "cp_passq_workspace_bytes", "cp_passq_decode", "cp_take_device_status",
+    "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
 ]
 
 CP_OK = 0
@@ -35,6 +35,7 @@ CP_MODE_EMIT = 0
 CP_MODE_ACCUMULATE = 1
 CP_MODE_FINALIZE = 2
 CP_MAX_MERGE_PARTS = 256
+CP_PASSQ_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -91,6 +92,7 @@ def load_library():
         "cp_passq_workspace_bytes": (_I32, [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]),
         "cp_passq_decode": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P]),
         "cp_take_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+        "cp_passq_decode_noalloc": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -198,6 +200,23 @@ def cp_passq_decode(desc: AttnDesc, q, k, v, workspace, workspace_bytes: int, ou
     st = lib.cp_passq_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(workspace),
                              int(workspace_bytes), _ptr(out), _ptr(m_out), _ptr(l_out), _stream(stream))
     _check(st, "cp_passq_decode")
+
+
+def cp_passq_decode_noalloc(desc: AttnDesc, q, k, v, out, m_out=None, l_out=None, stream=None) -> None:
+    """Pass-Q decode without a workspace, for callers that cannot allocate device memory.
+
+    The partials go to the library's fixed scratch of CP_PASSQ_NOALLOC_SCRATCH_BYTES
+    (8 MiB per GPU, held until exit).  Calls share that scratch: do not let two of
+    them overlap on the GPU.  A problem too large for it raises CpError with
+    CP_ERR_UNSUPPORTED before anything is launched.
+    """
+    lib = load_library()
+    st = lib.cp_passq_decode_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(m_out),
+                                     _ptr(l_out), _stream(stream))
+    if st == CP_ERR_UNSUPPORTED:
+        raise CpError(st, "cp_passq_decode_noalloc (unsupported shape, or partials larger than the "
+                          f"{CP_PASSQ_NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)")
+    _check(st, "cp_passq_decode_noalloc")
 
 
 def cp_take_device_status(stream=None) -> int:

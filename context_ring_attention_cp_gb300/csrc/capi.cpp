@@ -223,6 +223,48 @@ cp_status cp_passq_decode(const cp_attn_desc* desc, const void* q, const void* k
   return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
+cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
+                                  float* out, float* m_out, float* l_out, void* cuda_stream) {
+  cp_status st = check_decode_desc(desc);
+  if (st != CP_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return CP_ERR_INVALID_ARGUMENT;
+  if ((m_out != nullptr && !aligned16(m_out)) || (l_out != nullptr && !aligned16(l_out)))
+    return CP_ERR_INVALID_ARGUMENT;
+  int sms = 0;
+  if (current_sm_count(&sms) != cudaSuccess) return CP_ERR_CUDA;
+  // Same split of the shards as cp_passq_decode while the partials fit the fixed
+  // scratch; fewer splits (halving keeps them dividing the shard) otherwise.
+  const size_t cap = decode_noalloc_scratch_bytes();
+  int32_t splits = decode_splits_per_shard(*desc, sms);
+  while (splits > 1 && decode_workspace_bytes(*desc, splits) > cap) splits /= 2;
+  if (decode_workspace_bytes(*desc, splits) > cap) return CP_ERR_UNSUPPORTED;
+  const int64_t n_parts = desc->cp * splits;
+  if (n_parts > CP_MAX_MERGE_PARTS) return CP_ERR_UNSUPPORTED;
+  float* scratch = nullptr;
+  if (decode_noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
+  float *o_parts = nullptr, *m_parts = nullptr, *l_parts = nullptr;
+  decode_workspace_sections(*desc, splits, scratch, &o_parts, &m_parts, &l_parts);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  if (launch_decode_partials(*desc, splits, q, k, v, o_parts, m_parts, l_parts, s) != cudaSuccess)
+    return CP_ERR_CUDA;
+  MergeParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = desc->b;
+  p.rows = 1;
+  p.heads = desc->h_q;
+  p.d = desc->d;
+  p.n_parts = static_cast<int32_t>(n_parts);
+  p.finalize = 1;
+  p.o_parts = o_parts;
+  p.m_parts = m_parts;
+  p.l_parts = l_parts;
+  p.o_out = out;
+  p.m_out = m_out;
+  p.l_out = l_out;
+  for (int32_t i = 0; i < p.n_parts; ++i) p.order[i] = static_cast<uint16_t>(i);
+  return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
 cp_status cp_take_device_status(void* cuda_stream, int32_t* status) {
   if (status == nullptr) return CP_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CP_ERR_CUDA;

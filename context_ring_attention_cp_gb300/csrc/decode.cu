@@ -23,6 +23,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace cpattn {
@@ -305,6 +307,51 @@ cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const 
   CP_DEC(512, 1) CP_DEC(512, 2)
 #undef CP_DEC
   return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for cp_passq_decode_noalloc
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// a plug-in whose host runtime owns all of HBM and hands it only the input and
+// output buffers, or a latency-bound token loop that must not call cudaMalloc
+// (which may synchronise the device).  For them the decode partials live in this
+// array instead of a caller workspace.  It is part of the module image, so every
+// GPU that loads the library holds kNoAllocScratchBytes until the process exits.
+// All calls share it and it keeps the last call's contents; nothing in it needs
+// to start at zero (every partial is written before the reduce reads it), and
+// calls that overlap on the GPU race on it.
+
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = size_t(2) << 20;  // 8 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+}  // namespace
+
+size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchFloats * sizeof(float); }
+
+// The array's name in host code is only a host-side stand-in; the device
+// address is looked up once per device, with that device current.
+cudaError_t decode_noalloc_scratch(float** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace cpattn

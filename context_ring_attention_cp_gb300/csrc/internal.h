@@ -37,6 +37,11 @@ cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const 
                                    const void* k, const void* v, float* o_parts,
                                    float* m_parts, float* l_parts, cudaStream_t stream);
 
+// Fixed 8 MiB device scratch used by cp_passq_decode_noalloc (decode.cu): its size,
+// and its device address on the current device (looked up once per device).
+size_t decode_noalloc_scratch_bytes();
+cudaError_t decode_noalloc_scratch(float** ptr);
+
 // ---- ring-step attention (ring_attn.cu) ------------------------------------
 bool ring_supported(const cp_attn_desc& d);
 // Returns CP_OK, or CP_ERR_CUDA when a tensor map cannot be encoded or the launch fails.

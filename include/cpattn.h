@@ -169,6 +169,33 @@ CPATTN_API cp_status cp_passq_decode(const cp_attn_desc* desc, const void* q, co
                           const void* v, float* workspace, size_t workspace_bytes,
                           float* out, float* m_out, float* l_out, void* cuda_stream);
 
+/*
+ * Pass-Q decode that allocates nothing (the pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory).
+ * Same operation, layouts, support limits and argument errors as cp_passq_decode,
+ * but without a workspace argument: the per-range partial triples go to a fixed
+ * scratch array of CP_PASSQ_NOALLOC_SCRATCH_BYTES built into the library, which
+ * every GPU that loads the library holds until the process exits.  Callers that
+ * cannot allocate are, for example, a plug-in whose host runtime owns all device
+ * memory and hands it only its input and output buffers, or a token loop that
+ * must not call cudaMalloc because it may synchronise the device.
+ * - It calls no cudaMalloc, cudaFree or other allocating routine.
+ * - The first call on a device looks up the scratch's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - All calls share the scratch, which keeps the last call's contents (nothing in
+ *   it needs to start at zero).  Calls that overlap on the GPU (other streams,
+ *   or other host threads) race on it and must be serialised by the caller.
+ * - The shards are split as in cp_passq_decode while the partials fit; otherwise
+ *   into fewer ranges.  A problem whose partials do not fit even one range per
+ *   shard (cp * b * h_q * (d + 2) * 4 bytes, rounded up per section, above the
+ *   limit) returns CP_ERR_UNSUPPORTED before any launch.
+ */
+#define CP_PASSQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+CPATTN_API cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const void* k,
+                                             const void* v, float* out, float* m_out, float* l_out,
+                                             void* cuda_stream);
+
 /* Inputs of the closed-form byte counts (all >= 0; cp >= 1). */
 typedef struct {
   int64_t S;       /* sequence length */
