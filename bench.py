@@ -370,6 +370,24 @@ def bench_ours(args, rank, world, dist):
 def secondary_lines(cpa, synth, peaks, stream):
     import torch
     out = {}
+    # long prefill: b1, 32/8 heads, d128, S131072, cp16 (one fused ring launch, 140.7 TFLOP)
+    w = synth.WORKLOADS["long"]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+    l = torch.empty_like(m)
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    mode = cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE
+    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, stream)  # noqa: E731
+    fn()
+    ms = _events_time(fn, 3, stream)
+    tf = prefill_flops(w) / (ms * 1e-3) / 1e12
+    out["prefill_long"] = {"workload": "prefill ring attention, long: b1, 32/8 heads, d128, S131072, cp16",
+                           "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 3), "flops": prefill_flops(w),
+                           "peak": peaks["bf16_tflops_sustained"],
+                           "frac": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
     # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)
     w = synth.WORKLOADS["decode"]
     q, k, v = synth.decode_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], seed=w["seed"])
