@@ -309,6 +309,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Blackwell paired fp32 arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Three-input max.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -437,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     }
     for (int tt = 0; tt < 2; ++tt) {
       mbar_init(bar_s(tt), 1);
-      mbar_init(bar_p(tt), BM);
+      mbar_init(bar_p(tt), BM / 32);
       mbar_init(bar_o(tt), 1);
     }
     // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
@@ -617,17 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           x[i] = vis ? x[i] : -INFINITY;
         }
       }
-      // Row max with eight independent chains (short dependency depth).
+      // Row max: eight independent chains of three-input max (short dependency depth).
       float mx8[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx8[a] = x[a];
+      for (int a = 0; a < 8; ++a) {
+        mx8[a] = fmaxf(x[a], x[a + 8]);
 #pragma unroll
-      for (int i = 8; i < BN; i += 8) {
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], x[i + a]);
+        for (int kk = 2; kk < BN / 8; kk += 2) mx8[a] = max3(mx8[a], x[a + 8 * kk], x[a + 8 * kk + 8]);
       }
-      const float tmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.sl;
+      const float tmax = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], max3(mx8[5], mx8[6], mx8[7]))) *
+                         p.sl;
       m_true = fmaxf(m_true, tmax);
       // Raise the exponent reference only when the max grew by more than the threshold.
       const bool raise = tmax > m_ref + kRescaleThreshold;
@@ -639,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         m_ref = m_new;
       }
       const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      // p = 2^(x*sl - m_ref): paired FFMA, MUFU ex2, paired adds into four pair accumulators.
       float ps8[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) ps8[a] = 0.f;
@@ -647,10 +670,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = ex2(fmaf(x[c * 32 + 2 * i], p.sl, nmu));
-          const float b = ex2(fmaf(x[c * 32 + 2 * i + 1], p.sl, nmu));
-          ps8[(2 * i) % 8] += a;
-          ps8[(2 * i + 1) % 8] += b;
+          float ya, yb;
+          fma2(ya, yb, x[c * 32 + 2 * i], x[c * 32 + 2 * i + 1], p.sl, p.sl, nmu, nmu);
+          const float a = ex2(ya);
+          const float b = ex2(yb);
+          const int acc = (2 * i) % 8;
+          add2(ps8[acc], ps8[acc + 1], ps8[acc], ps8[acc + 1], a, b);
           pk[i] = pack_bf16(a, b);
         }
         tmem_st16(s_addr + uint32_t(c * 16), pk);
@@ -673,7 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       l_run += psum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p(tt));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(tt));  // one arrival per warp (count 4)
     }
 
     // ---------------- epilogue: this row's triple, merged / normalised as asked
