@@ -214,6 +214,22 @@ def run_oracle_pool(tasks, workers):
 # GPU arms
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(x: float, dist) -> float:
+    """The largest value of ``x`` over all ranks (the slowest rank's time)."""
+    if dist is None:
+        return float(x)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: int, world: int, steps: int, total_ms: float) -> float:
+    """Aggregate throughput: the work of every rank over the slowest rank's time."""
+    return flops_per_rank_step * world * steps / (total_ms * 1e-3) / 1e12
+
+
 def _events_time(fn, iters, stream):
     import torch
     start = torch.cuda.Event(enable_timing=True)
@@ -287,12 +303,9 @@ def bench_ours(args, rank, world, dist):
     kernel_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
     if cpa.cp_take_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, args.steps, total_ms)
 
     kern_ms = statistics.mean(kernel_ms)
     achieved = flops / (kern_ms * 1e-3) / 1e12
@@ -370,6 +383,27 @@ def bench_ours(args, rank, world, dist):
 def secondary_lines(cpa, synth, peaks, stream):
     import torch
     out = {}
+    # one ring step (t = 1) of all cp virtual ranks on the GQA workload, EMIT: the spec's
+    # per-step unit of work, cp * 2C^2 visible pairs per head (F_attn / cp per step in all)
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+    l = torch.empty_like(m)
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, cpa.CP_MODE_EMIT, stream)  # noqa
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 20, stream)
+    C = w["S"] // (2 * w["cp"])
+    step_flops = 4 * w["b"] * w["h_q"] * w["d"] * w["cp"] * 2 * C * C
+    tf = step_flops / (ms * 1e-3) / 1e12
+    out["prefill_one_step_emit"] = {
+        "workload": "one ring step (t=1, all 8 virtual ranks, EMIT) of the GQA prefill workload",
+        "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
+        "peak": peaks["bf16_tflops_sustained"], "frac": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
     # long prefill: b1, 32/8 heads, d128, S131072, cp16 (one fused ring launch, 140.7 TFLOP)
     w = synth.WORKLOADS["long"]
     q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
