@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "c93a0a01dcc05625", "bytes": 2258198728}
+RING_TRAFFIC = {"sha256_prefix": "0daa7873e1af22f5", "bytes": 2252896752}
 
 
 def ring_traffic():
