@@ -492,6 +492,40 @@ def bench_reference(args, rank, world):
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case(name, steps):
+    """One kernel on a capture-sized case (a few GB on the device) for ncu; prints its time."""
+    import torch
+    import context_ring_attention_cp_gb300 as cpa
+    from context_ring_attention_cp_gb300 import _build, synth
+    _build.build()
+    cpa.load_library()
+    stream = torch.cuda.current_stream()
+    if name == "decode-small":  # b8, 16 heads, d512, L8192, cp8: 2.1 GB of K/V
+        b, L, h, d, cp = 8, 8192, 16, 512, 8
+        q, k, v = synth.decode_inputs(b, L, h, h, d, seed=7)
+        desc = cpa.make_desc(b, L, h, h, d, cp, 1.0 / math.sqrt(d), 0)
+        nbytes = cpa.cp_passq_workspace_bytes(desc)
+        ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        out = torch.empty((b, h, d), dtype=torch.float32, device="cuda")
+        fn = lambda: cpa.cp_passq_decode(desc, q, k, v, ws, nbytes, out, None, None, stream)  # noqa: E731
+        work = 2 * b * L * h * d * 2
+    elif name == "merge":  # the merge-stress workload itself: 4.5 GB
+        w = synth.WORKLOADS["merge"]
+        po, pm, pl = synth.merge_parts(w["parts"], w["heads"], w["rows"], w["d"], spread=w["spread"], seed=w["seed"])
+        mo = torch.empty((1, w["rows"], w["heads"], w["d"]), dtype=torch.float32, device="cuda")
+        mm = torch.empty((1, w["heads"], w["rows"]), dtype=torch.float32, device="cuda")
+        ml = torch.empty_like(mm)
+        fn = lambda: cpa.cp_merge_partials(1, w["rows"], w["heads"], w["d"], w["parts"], po, pm, pl, mo, mm, ml,  # noqa
+                                           stream=stream)
+        work = merge_bytes(w)
+    else:
+        raise SystemExit(f"unknown --case {name}")
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, steps, stream)
+    print(json.dumps({"case": name, "ms": round(ms, 4), "GB/s": round(work / (ms * 1e-3) / 1e9, 1)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -503,7 +537,13 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--case", choices=["decode-small", "merge"], default=None,
+                    help="time one kernel on a capture-sized case (for ncu) instead of the benchmark")
     args = ap.parse_args()
+    if args.case is not None:
+        sys.path.insert(0, ROOT)
+        profile_case(args.case, args.steps)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     sys.path.insert(0, ROOT)
