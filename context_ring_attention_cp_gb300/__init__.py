@@ -59,12 +59,12 @@ class AttnDesc(ctypes.Structure):
 
 
 class _CommQuery(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int64) for n in ("S", "cp", "c_kv", "b", "d", "n_h", "s_dtype")]
+    _fields_ = [(n, ctypes.c_int64) for n in ("S", "cp", "c_kv", "b", "d", "n_h", "s_dtype", "layers_local")]
 
 
 class _CommResult(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("passkv_total", "passkv_per_step", "passq_dispatch",
-                                               "passq_reduce")]
+                                               "passq_reduce", "kv_bytes_per_rank")]
 
 
 _P = ctypes.c_void_p
@@ -150,14 +150,15 @@ def cp_plan_balanced_chunks(S: int, cp: int) -> dict:
             "step_pairs": step_pairs}
 
 
-def cp_comm_bytes(S, cp, c_kv, b=0, d=0, n_h=0, s_dtype=0) -> dict:
-    """Closed-form pass-KV / pass-Q byte counts (host, exact uint64)."""
+def cp_comm_bytes(S, cp, c_kv, b=0, d=0, n_h=0, s_dtype=0, layers_local=0) -> dict:
+    """Closed-form pass-KV / pass-Q byte counts and per-rank KV footprint (host, exact uint64)."""
     lib = load_library()
-    q = _CommQuery(int(S), int(cp), int(c_kv), int(b), int(d), int(n_h), int(s_dtype))
+    q = _CommQuery(int(S), int(cp), int(c_kv), int(b), int(d), int(n_h), int(s_dtype), int(layers_local))
     r = _CommResult()
     _check(lib.cp_comm_bytes(ctypes.byref(q), ctypes.byref(r)), "cp_comm_bytes")
     return {"passkv_total": int(r.passkv_total), "passkv_per_step": int(r.passkv_per_step),
-            "passq_dispatch": int(r.passq_dispatch), "passq_reduce": int(r.passq_reduce)}
+            "passq_dispatch": int(r.passq_dispatch), "passq_reduce": int(r.passq_reduce),
+            "kv_bytes_per_rank": int(r.kv_bytes_per_rank)}
 
 
 def cp_ring_step_partial_attn(desc: AttnDesc, step_begin: int, step_end: int, q, k, v, o, m, l,

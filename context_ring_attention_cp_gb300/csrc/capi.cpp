@@ -93,7 +93,8 @@ cp_status cp_plan_balanced_chunks(int64_t S, int32_t cp, int64_t* chunk_begin,
 
 cp_status cp_comm_bytes(const cp_comm_query* q, cp_comm_result* res) {
   if (q == nullptr || res == nullptr) return CP_ERR_INVALID_ARGUMENT;
-  if (q->S < 0 || q->cp < 1 || q->c_kv < 0 || q->b < 0 || q->d < 0 || q->n_h < 0 || q->s_dtype < 0)
+  if (q->S < 0 || q->cp < 1 || q->c_kv < 0 || q->b < 0 || q->d < 0 || q->n_h < 0 || q->s_dtype < 0 ||
+      q->layers_local < 0)
     return CP_ERR_INVALID_ARGUMENT;
   if (q->S % q->cp != 0) return CP_ERR_INVALID_ARGUMENT;
   uint64_t per_step, total, dispatch, width, reduce;
@@ -108,10 +109,16 @@ cp_status cp_comm_bytes(const cp_comm_query* q, cp_comm_result* res) {
       __builtin_mul_overflow(uint64_t(q->b), width, &reduce) ||
       __builtin_mul_overflow(reduce, uint64_t(q->s_dtype), &reduce))
     return CP_ERR_OVERFLOW;
+  uint64_t kv_rank;
+  if (__builtin_mul_overflow(uint64_t(q->b), tokens, &kv_rank) ||
+      __builtin_mul_overflow(kv_rank, uint64_t(q->c_kv), &kv_rank) ||
+      __builtin_mul_overflow(kv_rank, uint64_t(q->layers_local), &kv_rank))
+    return CP_ERR_OVERFLOW;
   res->passkv_total = total;
   res->passkv_per_step = per_step;
   res->passq_dispatch = dispatch;
   res->passq_reduce = reduce;
+  res->kv_bytes_per_rank = kv_rank;
   return CP_OK;
 }
 

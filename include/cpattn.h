@@ -205,6 +205,7 @@ typedef struct {
   int64_t d;       /* model hidden size (length of the partial output vector) */
   int64_t n_h;     /* attention heads */
   int64_t s_dtype; /* bytes per element of the pass-Q messages */
+  int64_t layers_local; /* attention layers held by one rank (L_local of the memory paragraph) */
 } cp_comm_query;
 
 typedef struct {
@@ -212,11 +213,14 @@ typedef struct {
   uint64_t passkv_per_step; /* (S/cp) * c_kv                 bytes of one ring step */
   uint64_t passq_dispatch;  /* b * d * s_dtype               pass-Q query dispatch */
   uint64_t passq_reduce;    /* b * (d + 2 n_h) * s_dtype     pass-Q reduce message */
+  uint64_t kv_bytes_per_rank; /* b * S * c_kv * L_local / cp  per-rank KV footprint */
 } cp_comm_result;
 
 /*
- * Closed-form communication volumes (Algorithm/formulas section: eq.
- * g5cp-passkv-bytes and the pass-Q paragraph), exact in uint64.  Host-only.
+ * Closed-form communication volumes and the per-rank KV footprint (Algorithm /
+ * formulas section: eq. g5cp-passkv-bytes, the pass-Q paragraph and the memory
+ * paragraph), exact in uint64.  Host-only.  The footprint is computed as
+ * b * (S/cp) * c_kv * L_local, exact because S % cp == 0.
  * The pass-KV formula carries no batch factor, as printed (per rank per layer).
  * Errors: NULL pointer, a negative field, cp < 1, S % cp != 0 ->
  * CP_ERR_INVALID_ARGUMENT; any result above 2^64-1 -> CP_ERR_OVERFLOW (the

@@ -94,6 +94,20 @@ def test_comm_bytes_bit_exact_against_oracle(cpa, case):
     assert (got["passq_dispatch"], got["passq_reduce"]) == (disp, red)
 
 
+@pytest.mark.parametrize("b,S,cp,c_kv,L", [(1, 1 << 20, 8, 320, 61), (1, 1 << 20, 16, 320, 61), (8, 131072, 8, 16384, 1),
+                                             (2, 96, 4, 3, 5), (1, 64, 1, 8, 0)])
+def test_kv_bytes_per_rank_bit_exact(cpa, b, S, cp, c_kv, L):
+    got = cpa.cp_comm_bytes(S, cp, c_kv, b=b, layers_local=L)["kv_bytes_per_rank"]
+    assert got == OC.kv_bytes_per_rank(b, S, c_kv, L, cp)
+
+
+def test_kv_per_rank_halves_from_cp8_to_cp16(cpa):
+    # use case section: raising cp from 8 to 16 halves the KV each card holds
+    a = cpa.cp_comm_bytes(1 << 20, 8, 320, b=1, layers_local=61)["kv_bytes_per_rank"]
+    c = cpa.cp_comm_bytes(1 << 20, 16, 320, b=1, layers_local=61)["kv_bytes_per_rank"]
+    assert 2 * c == a
+
+
 def test_comm_bytes_at_the_workloads(cpa):
     # c_kv for grouped-query attention: K and V, h_kv heads of d_head bf16 values
     for S, cp, hkv, dh in [(1024, 2, 4, 64), (32768, 8, 8, 128), (131072, 16, 8, 128)]:
@@ -121,6 +135,12 @@ def test_comm_bytes_overflow_and_errors(cpa):
     with pytest.raises(cpa.CpError) as e:
         cpa.cp_comm_bytes(10, 1, 1, b=-1)
     assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_comm_bytes(10, 1, 1, layers_local=-1)
+    assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:  # footprint overflows even though the ring bytes fit
+        cpa.cp_comm_bytes(1 << 40, 1, 1 << 10, b=1 << 20, layers_local=1)
+    assert e.value.status == 3
 
 
 # --- device entry points: argument errors only (rejected before any CUDA call) ---
