@@ -404,6 +404,30 @@ def secondary_lines(cpa, synth, peaks, stream):
         "peak": peaks["bf16_tflops_sustained"], "frac": round(tf / peaks["bf16_tflops_sustained"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
+    # per-virtual-rank work under the balanced (method) and sequential (plain) layouts:
+    # one launch per rank covering all its ring steps
+    w = synth.WORKLOADS[WORKLOAD]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+    l = torch.empty_like(m)
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    balance = {}
+    for name, layout in (("balanced", cpa.CP_LAYOUT_BALANCED), ("sequential", cpa.CP_LAYOUT_SEQUENTIAL)):
+        pairs = cpa.cp_plan_chunks(w["S"], w["cp"], layout)["step_pairs"].sum(axis=1)
+        times = []
+        for r in range(w["cp"]):
+            fn = lambda: cpa.cp_ring_rank_partial_attn(desc, layout, r, r + 1, 0, w["cp"], q, k, v, o, m, l,  # noqa
+                                                       cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE, stream)
+            fn()
+            times.append(_events_time(fn, 3, stream))
+        balance[name] = {"rank_ms": [round(x, 4) for x in times],
+                         "max_over_min_ms": round(max(times) / min(times), 3),
+                         "rank_pairs_per_head": [int(x) for x in pairs],
+                         "max_over_min_pairs": round(float(pairs.max() / pairs.min()), 3)}
+    out["rank_balance"] = {"workload": "GQA prefill, one launch per virtual rank (all its ring steps)", **balance}
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
     # long prefill: b1, 32/8 heads, d128, S131072, cp16 (one fused ring launch, 140.7 TFLOP)
     w = synth.WORKLOADS["long"]
     q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])

@@ -21,7 +21,8 @@ import numpy as np
 __all__ = [
     "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE",
     "CP_MAX_MERGE_PARTS", "library_path", "load_library", "cp_status_string",
-    "cp_plan_balanced_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn", "cp_merge_partials",
+    "cp_plan_balanced_chunks", "cp_plan_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn",
+    "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
 ]
 
@@ -34,6 +35,8 @@ CP_ERR_TIMEOUT = 5
 CP_MODE_EMIT = 0
 CP_MODE_ACCUMULATE = 1
 CP_MODE_FINALIZE = 2
+CP_LAYOUT_BALANCED = 0
+CP_LAYOUT_SEQUENTIAL = 1
 CP_MAX_MERGE_PARTS = 256
 CP_PASSQ_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -85,6 +88,9 @@ def load_library():
     sig = {
         "cp_status_string": (ctypes.c_char_p, [_I32]),
         "cp_plan_balanced_chunks": (_I32, [_I64, _I32, _P, _P, _P, _P]),
+        "cp_plan_chunks": (_I32, [_I64, _I32, _I32, _P, _P, _P, _P]),
+        "cp_ring_rank_partial_attn": (_I32, [ctypes.POINTER(AttnDesc), _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P,
+                                             _P, _P, _I32, _P]),
         "cp_comm_bytes": (_I32, [ctypes.POINTER(_CommQuery), ctypes.POINTER(_CommResult)]),
         "cp_ring_step_partial_attn": (_I32, [ctypes.POINTER(AttnDesc), _I32, _I32, _P, _P, _P, _P, _P, _P,
                                              _I32, _P]),
@@ -134,7 +140,12 @@ def make_desc(b, S, h_q, h_kv, d, cp, scale, causal) -> AttnDesc:
 
 
 def cp_plan_balanced_chunks(S: int, cp: int) -> dict:
-    """Host planner; returns the four plan arrays as numpy arrays."""
+    """Host planner (balanced layout); returns the four plan arrays as numpy arrays."""
+    return cp_plan_chunks(S, cp, CP_LAYOUT_BALANCED, _name="cp_plan_balanced_chunks")
+
+
+def cp_plan_chunks(S: int, cp: int, layout: int = CP_LAYOUT_BALANCED, _name: str = "cp_plan_chunks") -> dict:
+    """Host planner for either chunk layout; returns the four plan arrays as numpy arrays."""
     lib = load_library()
     if not isinstance(cp, (int, np.integer)) or cp < 1 or cp > (1 << 20):
         # the arrays below are sized by cp: reject before allocating (the library checks again)
@@ -143,9 +154,13 @@ def cp_plan_balanced_chunks(S: int, cp: int) -> dict:
     rank_chunks = np.zeros((cp, 2), np.int32)
     step_src = np.zeros((cp, cp), np.int32)
     step_pairs = np.zeros((cp, cp), np.int64)
-    st = lib.cp_plan_balanced_chunks(int(S), int(cp), chunk_begin.ctypes.data, rank_chunks.ctypes.data,
-                                     step_src.ctypes.data, step_pairs.ctypes.data)
-    _check(st, "cp_plan_balanced_chunks")
+    if _name == "cp_plan_balanced_chunks":
+        st = lib.cp_plan_balanced_chunks(int(S), int(cp), chunk_begin.ctypes.data, rank_chunks.ctypes.data,
+                                         step_src.ctypes.data, step_pairs.ctypes.data)
+    else:
+        st = lib.cp_plan_chunks(int(S), int(cp), int(layout), chunk_begin.ctypes.data, rank_chunks.ctypes.data,
+                                step_src.ctypes.data, step_pairs.ctypes.data)
+    _check(st, _name)
     return {"chunk_begin": chunk_begin, "rank_chunks": rank_chunks, "step_src": step_src,
             "step_pairs": step_pairs}
 
@@ -168,6 +183,16 @@ def cp_ring_step_partial_attn(desc: AttnDesc, step_begin: int, step_end: int, q,
     st = lib.cp_ring_step_partial_attn(ctypes.byref(desc), int(step_begin), int(step_end), _ptr(q), _ptr(k),
                                        _ptr(v), _ptr(o), _ptr(m), _ptr(l), int(mode), _stream(stream))
     _check(st, "cp_ring_step_partial_attn")
+
+
+def cp_ring_rank_partial_attn(desc: AttnDesc, layout: int, rank_begin: int, rank_end: int, step_begin: int,
+                              step_end: int, q, k, v, o, m, l, mode: int = CP_MODE_EMIT, stream=None) -> None:
+    """Ring steps [step_begin, step_end) for the virtual ranks [rank_begin, rank_end) under a layout."""
+    lib = load_library()
+    st = lib.cp_ring_rank_partial_attn(ctypes.byref(desc), int(layout), int(rank_begin), int(rank_end),
+                                       int(step_begin), int(step_end), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m),
+                                       _ptr(l), int(mode), _stream(stream))
+    _check(st, "cp_ring_rank_partial_attn")
 
 
 def cp_merge_partials(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out,

@@ -69,26 +69,44 @@ const char* cp_status_string(int32_t status) {
   }
 }
 
-cp_status cp_plan_balanced_chunks(int64_t S, int32_t cp, int64_t* chunk_begin,
-                                  int32_t* rank_chunks, int32_t* step_src,
-                                  int64_t* step_pairs) {
+cp_status cp_plan_chunks(int64_t S, int32_t cp, int32_t layout, int64_t* chunk_begin, int32_t* rank_chunks,
+                         int32_t* step_src, int64_t* step_pairs) {
   if (cp < 1 || S < 1 || cp > (1 << 20)) return CP_ERR_INVALID_ARGUMENT;
   if (S % (2 * int64_t(cp)) != 0) return CP_ERR_INVALID_ARGUMENT;
+  if (layout != CP_LAYOUT_BALANCED && layout != CP_LAYOUT_SEQUENTIAL) return CP_ERR_INVALID_ARGUMENT;
   if (!chunk_begin || !rank_chunks || !step_src || !step_pairs) return CP_ERR_INVALID_ARGUMENT;
   const int64_t C = S / (2 * int64_t(cp));
-  int64_t pairs_off = 0, pairs_diag = 0;
-  if (__builtin_mul_overflow(2 * C, C, &pairs_off) || __builtin_add_overflow(pairs_off, C, &pairs_diag))
+  const int64_t n = 2 * C;  // rows per rank
+  int64_t pairs_off = 0, pairs_diag = 0, seq_full = 0, seq_tri = 0;
+  if (__builtin_mul_overflow(2 * C, C, &pairs_off) || __builtin_add_overflow(pairs_off, C, &pairs_diag) ||
+      __builtin_mul_overflow(n, n, &seq_full) || __builtin_mul_overflow(n, n + 1, &seq_tri))
     return CP_ERR_OVERFLOW;
+  seq_tri /= 2;
   for (int64_t kk = 0; kk <= 2 * int64_t(cp); ++kk) chunk_begin[kk] = kk * C;
   for (int32_t r = 0; r < cp; ++r) {
-    rank_chunks[2 * r] = r;               // head chunk
-    rank_chunks[2 * r + 1] = 2 * cp - 1 - r;  // tail chunk
+    if (layout == CP_LAYOUT_BALANCED) {
+      rank_chunks[2 * r] = r;                   // head chunk
+      rank_chunks[2 * r + 1] = 2 * cp - 1 - r;  // tail chunk
+    } else {
+      rank_chunks[2 * r] = 2 * r;
+      rank_chunks[2 * r + 1] = 2 * r + 1;
+    }
     for (int32_t t = 0; t < cp; ++t) {
-      step_src[int64_t(r) * cp + t] = ((r - t) % cp + cp) % cp;
-      step_pairs[int64_t(r) * cp + t] = (t == 0) ? pairs_diag : pairs_off;
+      const int32_t s = ((r - t) % cp + cp) % cp;
+      step_src[int64_t(r) * cp + t] = s;
+      if (layout == CP_LAYOUT_BALANCED)
+        step_pairs[int64_t(r) * cp + t] = (t == 0) ? pairs_diag : pairs_off;
+      else  // sequential: earlier source fully visible, own block causal, later source nothing
+        step_pairs[int64_t(r) * cp + t] = (s < r) ? seq_full : (s == r ? seq_tri : 0);
     }
   }
   return CP_OK;
+}
+
+cp_status cp_plan_balanced_chunks(int64_t S, int32_t cp, int64_t* chunk_begin,
+                                  int32_t* rank_chunks, int32_t* step_src,
+                                  int64_t* step_pairs) {
+  return cp_plan_chunks(S, cp, CP_LAYOUT_BALANCED, chunk_begin, rank_chunks, step_src, step_pairs);
 }
 
 cp_status cp_comm_bytes(const cp_comm_query* q, cp_comm_result* res) {
@@ -122,21 +140,33 @@ cp_status cp_comm_bytes(const cp_comm_query* q, cp_comm_result* res) {
   return CP_OK;
 }
 
-cp_status cp_ring_step_partial_attn(const cp_attn_desc* desc, int32_t step_begin,
-                                    int32_t step_end, const void* q, const void* k,
-                                    const void* v, float* o, float* m, float* l,
-                                    int32_t mode, void* cuda_stream) {
+cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t layout, int32_t rank_begin,
+                                    int32_t rank_end, int32_t step_begin, int32_t step_end, const void* q,
+                                    const void* k, const void* v, float* o, float* m, float* l, int32_t mode,
+                                    void* cuda_stream) {
   cp_status st = check_desc_common(desc);
   if (st != CP_OK) return st;
   if (desc->S % (2 * desc->cp) != 0) return CP_ERR_INVALID_ARGUMENT;
+  if (layout != CP_LAYOUT_BALANCED && layout != CP_LAYOUT_SEQUENTIAL) return CP_ERR_INVALID_ARGUMENT;
+  if (rank_begin < 0 || rank_end <= rank_begin || rank_end > desc->cp) return CP_ERR_INVALID_ARGUMENT;
   if (step_begin < 0 || step_end <= step_begin || step_end > desc->cp) return CP_ERR_INVALID_ARGUMENT;
   if ((mode & ~(CP_MODE_ACCUMULATE | CP_MODE_FINALIZE)) != 0) return CP_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(m) || !aligned16(l))
     return CP_ERR_INVALID_ARGUMENT;
   if (desc->causal != 1) return CP_ERR_UNSUPPORTED;
   if (!ring_supported(*desc)) return CP_ERR_UNSUPPORTED;
-  return launch_ring_attn(*desc, step_begin, step_end, q, k, v, o, m, l, mode,
+  return launch_ring_attn(*desc, layout, rank_begin, rank_end, step_begin, step_end, q, k, v, o, m, l, mode,
                           static_cast<cudaStream_t>(cuda_stream));
+}
+
+cp_status cp_ring_step_partial_attn(const cp_attn_desc* desc, int32_t step_begin,
+                                    int32_t step_end, const void* q, const void* k,
+                                    const void* v, float* o, float* m, float* l,
+                                    int32_t mode, void* cuda_stream) {
+  if (desc == nullptr) return CP_ERR_INVALID_ARGUMENT;
+  if (desc->cp < 1 || desc->cp > (1 << 20)) return CP_ERR_INVALID_ARGUMENT;
+  return cp_ring_rank_partial_attn(desc, CP_LAYOUT_BALANCED, 0, int32_t(desc->cp), step_begin, step_end, q, k, v,
+                                   o, m, l, mode, cuda_stream);
 }
 
 cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t d,

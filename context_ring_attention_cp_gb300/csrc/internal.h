@@ -45,9 +45,10 @@ cudaError_t decode_noalloc_scratch(float** ptr);
 // ---- ring-step attention (ring_attn.cu) ------------------------------------
 bool ring_supported(const cp_attn_desc& d);
 // Returns CP_OK, or CP_ERR_CUDA when a tensor map cannot be encoded or the launch fails.
-cp_status launch_ring_attn(const cp_attn_desc& d, int32_t step_begin, int32_t step_end,
-                           const void* q, const void* k, const void* v, float* o, float* m,
-                           float* l, int32_t mode, cudaStream_t stream);
+cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_begin, int32_t rank_end,
+                           int32_t step_begin, int32_t step_end, const void* q, const void* k,
+                           const void* v, float* o, float* m, float* l, int32_t mode,
+                           cudaStream_t stream);
 // Reads and clears the ring kernel's device status word (after the caller synchronised).
 cudaError_t ring_take_status(int32_t* status);
 

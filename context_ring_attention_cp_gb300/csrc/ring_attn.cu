@@ -12,6 +12,11 @@
 //  * eq. g5cp-step-flops: every (rank, step) holds the same 2*C^2 visible pairs
 //    (plus C on step 0), F_attn / cp^2.
 //
+// Layouts.  Balanced (the method): rank r owns chunks r and 2cp-1-r.  Sequential
+// (the plain split the spec contrasts it with, kept for measuring imbalance):
+// rank r owns chunks 2r and 2r+1.  A launch covers the ranks [rank_begin,
+// rank_end) and the steps [step_begin, step_end).
+//
 // Work decomposition.  One CTA owns one 128-row query tile of one chunk for up
 // to two query heads that share a kv head (grouped-query attention), and walks
 // the ring steps [step_begin, step_end) in order.  For each step it visits the
@@ -98,6 +103,7 @@ struct RingParams {
   int32_t group;      // h_q / h_kv
   int32_t step_begin, step_end;
   int32_t mode;
+  int32_t rank_begin, rank_end;  // virtual ranks whose rows this launch computes
   float sl;           // scale * log2(e)
 };
 
@@ -348,6 +354,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Ring schedule: the KV tiles one query tile visits over steps [t0, t1)
 // ---------------------------------------------------------------------------
 
+template <int LAYOUT>
 struct KvCursor {
   int32_t cp, r, c_q, t, t_end, half;
   int32_t C, q_last;
@@ -362,13 +369,14 @@ struct KvCursor {
     seg_diag = false;
   }
 
-  // Next non-empty chunk segment: per step the head chunk of the source rank,
-  // then its tail chunk.
+  // Next non-empty chunk segment: per step the first chunk of the source rank,
+  // then its second chunk (balanced: s and 2cp-1-s; sequential: 2s and 2s+1).
   __device__ void find() {
     seg_n = 0;
     while (t < t_end) {
       const int32_t s = ((r - t) % cp + cp) % cp;
-      const int32_t c = (half == 0) ? s : 2 * cp - 1 - s;
+      const int32_t c = (LAYOUT == CP_LAYOUT_SEQUENTIAL) ? (2 * s + half)
+                                                       : ((half == 0) ? s : 2 * cp - 1 - s);
       half ^= 1;
       if (half == 0) ++t;
       seg_i = 0;
@@ -405,9 +413,11 @@ struct Item {
   int32_t c_q, r, q_row0, q_rows;
 };
 
+template <int LAYOUT>
 __device__ __forceinline__ Item decode_item(const RingParams& p) {
   Item it;
-  const int32_t n_qt = 2 * p.cp * p.tpc;
+  const int32_t nr = p.rank_end - p.rank_begin;
+  const int32_t n_qt = 2 * nr * p.tpc;  // query tiles of the selected ranks
   const int64_t per_tile = p.b * p.n_pairs;
   const int64_t idx = blockIdx.x;
   const int32_t gq = n_qt - 1 - int32_t(idx / per_tile);  // latest chunk (most keys) first
@@ -418,11 +428,20 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t i = pair % p.ppg;
   it.h0 = it.kvh * p.group + 2 * i;
   it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
-  it.c_q = gq / p.tpc;
+  // a-th selected chunk in ascending order.  Balanced: the ranks' head chunks
+  // [rank_begin, rank_end) then their tail chunks [2cp-rank_end, 2cp-rank_begin);
+  // sequential: chunks [2 rank_begin, 2 rank_end).
+  const int32_t a = gq / p.tpc;
   const int32_t kq = gq % p.tpc;
+  if (LAYOUT == CP_LAYOUT_SEQUENTIAL) {
+    it.c_q = 2 * p.rank_begin + a;
+    it.r = it.c_q / 2;
+  } else {
+    it.c_q = (a < nr) ? p.rank_begin + a : 2 * p.cp - p.rank_end + (a - nr);
+    it.r = (it.c_q < p.cp) ? it.c_q : 2 * p.cp - 1 - it.c_q;
+  }
   it.q_row0 = it.c_q * p.C + BM * kq;
   it.q_rows = min(BM, p.C - BM * kq);
-  it.r = (it.c_q < p.cp) ? it.c_q : 2 * p.cp - 1 - it.c_q;
   return it;
 }
 
@@ -430,7 +449,7 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int D>
+template <int D, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_constant__ RingParams p) {
   using K = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const Item it = decode_item(p);
+  const Item it = decode_item<LAYOUT>(p);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -480,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   // Number of KV tiles this query tile visits over the step range.
   int32_t n_kv = 0;
   {
-    KvCursor cur;
+    KvCursor<LAYOUT> cur;
     cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
     int32_t k0, ke;
     bool dg;
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         for (int sl = 0; sl < K::kSlabs; ++sl)
           tma_load_4d(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
                       it.h0 + tt, it.q_row0, it.bi);
-      KvCursor cur;
+      KvCursor<LAYOUT> cur;
       cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
       int32_t key0, key_end;
       bool diag;
@@ -615,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     float l_run = 0.f;
     bool ok = true;
 
-    KvCursor cur;
+    KvCursor<LAYOUT> cur;
     cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
     for (int32_t j = 0; j < n_kv; ++j) {
       int32_t key0 = 0, key_end = 0;
@@ -806,13 +825,13 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int LAYOUT>
 cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
   using K = Cfg<D>;
-  if (cudaFuncSetAttribute(ring_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmemBytes) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(ring_attn_kernel<D, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           K::kSmemBytes) != cudaSuccess)
     return CP_ERR_CUDA;
-  ring_attn_kernel<D><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
+  ring_attn_kernel<D, LAYOUT><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
@@ -823,9 +842,9 @@ bool ring_supported(const cp_attn_desc& d) {
   return (d.d == 64 || d.d == 128) && d.S < (int64_t(1) << 30) && d.b <= 65535 && d.h_q <= 65535;
 }
 
-cp_status launch_ring_attn(const cp_attn_desc& d, int32_t step_begin, int32_t step_end, const void* q,
-                           const void* k, const void* v, float* o, float* m, float* l, int32_t mode,
-                           cudaStream_t stream) {
+cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_begin, int32_t rank_end,
+                           int32_t step_begin, int32_t step_end, const void* q, const void* k, const void* v,
+                           float* o, float* m, float* l, int32_t mode, cudaStream_t stream) {
   RingParams p;
   memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tmap_q, q, d.b, d.S, d.h_q, d.d) || !encode_map(&p.tmap_k, k, d.b, d.S, d.h_kv, d.d) ||
@@ -847,10 +866,16 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t step_begin, int32_t st
   p.step_begin = step_begin;
   p.step_end = step_end;
   p.mode = mode;
+  p.rank_begin = rank_begin;
+  p.rank_end = rank_end;
   p.sl = d.scale * kLog2e;
-  const int64_t n_items = int64_t(2) * p.cp * p.tpc * d.b * p.n_pairs;
+  const int64_t n_items = int64_t(2) * (rank_end - rank_begin) * p.tpc * d.b * p.n_pairs;
   if (n_items > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
-  return d.d == 128 ? launch_d<128>(p, n_items, stream) : launch_d<64>(p, n_items, stream);
+  if (layout == CP_LAYOUT_SEQUENTIAL)
+    return d.d == 128 ? launch_d<128, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream)
+                      : launch_d<64, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream);
+  return d.d == 128 ? launch_d<128, CP_LAYOUT_BALANCED>(p, n_items, stream)
+                    : launch_d<64, CP_LAYOUT_BALANCED>(p, n_items, stream);
 }
 
 cudaError_t ring_take_status(int32_t* status) {

@@ -60,6 +60,12 @@ enum {
   CP_MODE_FINALIZE = 2    /* after that, write o = O / l (0 where l = 0); m, l stay */
 };
 
+/* Chunk layouts.  BALANCED is the method (Terms table, "Balanced chunk split"):
+ * rank r holds chunks r and 2cp-1-r.  SEQUENTIAL is the plain split the same row
+ * contrasts it with (rank r holds tokens [r*S/cp, (r+1)*S/cp) = chunks 2r, 2r+1),
+ * provided to measure the imbalance the balanced split removes. */
+enum { CP_LAYOUT_BALANCED = 0, CP_LAYOUT_SEQUENTIAL = 1 };
+
 /* Largest number of partial triples one cp_merge_partials call merges. */
 #define CP_MAX_MERGE_PARTS 256
 
@@ -97,6 +103,16 @@ CPATTN_API cp_status cp_plan_balanced_chunks(int64_t S, int32_t cp, int64_t* chu
                                   int64_t* step_pairs);
 
 /*
+ * The same plan for either layout (cp_plan_balanced_chunks == layout BALANCED).
+ * SEQUENTIAL: rank_chunks[r] = {2r, 2r+1}; with n = S/cp rows per rank,
+ * step_pairs[r][t] = n^2 when the source rank s < r, n(n+1)/2 when s == r, 0 when
+ * s > r (per-rank totals differ: the imbalance the Terms table describes).
+ * Errors: as cp_plan_balanced_chunks, plus an unknown layout -> CP_ERR_INVALID_ARGUMENT.
+ */
+CPATTN_API cp_status cp_plan_chunks(int64_t S, int32_t cp, int32_t layout, int64_t* chunk_begin,
+                                    int32_t* rank_chunks, int32_t* step_src, int64_t* step_pairs);
+
+/*
  * Ring-step partial attention (Terms table rows "Pass-KV", "Ring step", "Partial
  * attention"; eq. g5cp-step-flops) for ALL cp virtual ranks at once, over the ring
  * steps [step_begin, step_end).  For every rank r, local query row i (global
@@ -118,6 +134,19 @@ CPATTN_API cp_status cp_ring_step_partial_attn(const cp_attn_desc* desc, int32_t
                                     int32_t step_end, const void* q, const void* k,
                                     const void* v, float* o, float* m, float* l,
                                     int32_t mode, void* cuda_stream);
+
+/*
+ * Ring-step partial attention for the virtual ranks [rank_begin, rank_end) only,
+ * under either chunk layout; cp_ring_step_partial_attn is layout BALANCED over all
+ * ranks [0, cp).  Only the selected ranks' rows of (o, m, l) are read or written.
+ * Used to time one virtual rank's work (the per-rank balance of a layout).
+ * Errors: as cp_ring_step_partial_attn, plus an unknown layout or
+ * 0 <= rank_begin < rank_end <= cp violated -> CP_ERR_INVALID_ARGUMENT.
+ */
+CPATTN_API cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t layout, int32_t rank_begin,
+                                               int32_t rank_end, int32_t step_begin, int32_t step_end,
+                                               const void* q, const void* k, const void* v, float* o, float* m,
+                                               float* l, int32_t mode, void* cuda_stream);
 
 /*
  * LSE merge of n_parts partial triples (Terms table, row "Partial attention":

@@ -47,9 +47,21 @@ def chunk_begin(S, cp):
     return [k * C for k in range(2 * cp + 1)]
 
 
-def rank_chunks(cp):
-    """Head and tail chunk of every rank: [[r, 2cp-1-r] for r in range(cp)]."""
-    return [[r, 2 * cp - 1 - r] for r in range(cp)]
+LAYOUTS = ("balanced", "sequential")
+
+
+def rank_chunks(cp, layout="balanced"):
+    """The two chunks of every rank.
+
+    balanced:   [r, 2cp-1-r]  (head/tail pairing, Terms table "Balanced chunk split")
+    sequential: [2r, 2r+1]    (the plain split the Terms table contrasts it with:
+                               rank r holds tokens [r*S/cp, (r+1)*S/cp))
+    """
+    if layout == "balanced":
+        return [[r, 2 * cp - 1 - r] for r in range(cp)]
+    if layout == "sequential":
+        return [[2 * r, 2 * r + 1] for r in range(cp)]
+    raise ValueError(f"unknown layout {layout!r}")
 
 
 def step_source(cp):
@@ -57,23 +69,23 @@ def step_source(cp):
     return [[(r - t) % cp for t in range(cp)] for r in range(cp)]
 
 
-def rank_rows(S, cp, r):
-    """Global row indices owned by rank r: head chunk then tail chunk."""
+def rank_rows(S, cp, r, layout="balanced"):
+    """Global row indices owned by rank r: its first chunk then its second chunk."""
     C = S // (2 * cp)
-    head, tail = r, 2 * cp - 1 - r
-    return np.concatenate([np.arange(head * C, (head + 1) * C),
-                           np.arange(tail * C, (tail + 1) * C)])
+    first, second = rank_chunks(cp, layout)[r]
+    return np.concatenate([np.arange(first * C, (first + 1) * C),
+                           np.arange(second * C, (second + 1) * C)])
 
 
-def step_pairs_enumerated(S, cp):
+def step_pairs_enumerated(S, cp, layout="balanced"):
     """Visible (query, key) pairs per (rank, step) for one head, counted one by one."""
     _check_plan_args(S, cp)
     src = step_source(cp)
     out = [[0] * cp for _ in range(cp)]
     for r in range(cp):
-        rows = rank_rows(S, cp, r)
+        rows = rank_rows(S, cp, r, layout)
         for t in range(cp):
-            keys = rank_rows(S, cp, src[r][t])
+            keys = rank_rows(S, cp, src[r][t], layout)
             out[r][t] = int((keys[None, :] <= rows[:, None]).sum())
     return out
 
@@ -89,6 +101,19 @@ def step_pairs_closed_form(S, cp):
     _check_plan_args(S, cp)
     C = S // (2 * cp)
     return [[2 * C * C + (C if t == 0 else 0) for t in range(cp)] for _ in range(cp)]
+
+
+def step_pairs_sequential_closed_form(S, cp):
+    """Visible pairs per (rank, step) under the sequential layout (n = S/cp rows per rank).
+
+    Source s < r: the whole n x n block is visible; s = r (step 0): the causal
+    triangle n(n+1)/2; s > r: nothing.
+    """
+    _check_plan_args(S, cp)
+    n = S // cp
+    src = step_source(cp)
+    return [[(n * n if src[r][t] < r else (n * (n + 1) // 2 if src[r][t] == r else 0)) for t in range(cp)]
+            for r in range(cp)]
 
 
 def sequential_split_pairs(S, cp):
@@ -160,7 +185,7 @@ def finalize(triple):
 # ring steps
 # ---------------------------------------------------------------------------
 
-def ring_step_triple(q, k, v, scale, cp, r, t):
+def ring_step_triple(q, k, v, scale, cp, r, t, layout="balanced"):
     """Partial triple of virtual rank r at ring step t, over its local rows.
 
     Rows: rank r's head chunk then tail chunk (global positions in
@@ -175,8 +200,8 @@ def ring_step_triple(q, k, v, scale, cp, r, t):
     _check_plan_args(S, cp)
     g = hq // hkv
     s = (r - t) % cp
-    rows = rank_rows(S, cp, r)
-    keys = rank_rows(S, cp, s)
+    rows = rank_rows(S, cp, r, layout)
+    keys = rank_rows(S, cp, s, layout)
     invisible = keys[None, :] > rows[:, None]
     n = rows.size
     m = np.empty((b, hq, n))
@@ -192,7 +217,7 @@ def ring_step_triple(q, k, v, scale, cp, r, t):
     return rows, m, l, o
 
 
-def ring_attention(q, k, v, scale, cp, steps=None):
+def ring_attention(q, k, v, scale, cp, steps=None, layout="balanced"):
     """Ring restatement: every rank merges its per-step triples in step order.
 
     ``steps`` (default all of 0..cp-1) selects which ring steps are merged.
@@ -208,10 +233,10 @@ def ring_attention(q, k, v, scale, cp, steps=None):
     l = np.zeros((b, hq, S))
     o = np.zeros((b, S, hq, d))
     for r in range(cp):
-        rows = rank_rows(S, cp, r)
+        rows = rank_rows(S, cp, r, layout)
         acc = (m[:, :, rows], l[:, :, rows], np.moveaxis(o[:, rows], 1, 2))
         for t in steps:
-            _, sm, sl, so = ring_step_triple(q, k, v, scale, cp, r, t)
+            _, sm, sl, so = ring_step_triple(q, k, v, scale, cp, r, t, layout)
             acc = merge(acc, (sm, sl, so))
         m[:, :, rows] = acc[0]
         l[:, :, rows] = acc[1]

@@ -34,9 +34,9 @@ def _declared_symbols():
 
 def test_header_declares_the_boundary():
     syms = _declared_symbols()
-    for name in ["cp_plan_balanced_chunks", "cp_ring_step_partial_attn", "cp_merge_partials",
-                 "cp_passq_decode", "cp_comm_bytes", "cp_passq_workspace_bytes", "cp_status_string",
-                 "cp_take_device_status"]:
+    for name in ["cp_plan_balanced_chunks", "cp_plan_chunks", "cp_ring_step_partial_attn",
+                 "cp_ring_rank_partial_attn", "cp_merge_partials", "cp_passq_decode", "cp_comm_bytes",
+                 "cp_passq_workspace_bytes", "cp_status_string", "cp_take_device_status"]:
         assert name in syms, name
 
 
@@ -62,6 +62,34 @@ def test_plan_bit_exact_against_oracle(cpa, S, cp):
     assert plan["step_pairs"].tolist() == OR.step_pairs_closed_form(S, cp)
     if S <= 128:
         assert plan["step_pairs"].tolist() == OR.step_pairs_enumerated(S, cp)
+
+
+@pytest.mark.parametrize("S,cp", [(2, 1), (16, 2), (24, 3), (64, 4), (96, 8), (32768, 8), (131072, 16)])
+def test_sequential_plan_bit_exact_against_oracle(cpa, S, cp):
+    plan = cpa.cp_plan_chunks(S, cp, cpa.CP_LAYOUT_SEQUENTIAL)
+    assert plan["chunk_begin"].tolist() == OR.chunk_begin(S, cp)
+    assert plan["rank_chunks"].tolist() == OR.rank_chunks(cp, "sequential")
+    assert plan["step_src"].tolist() == OR.step_source(cp)
+    assert plan["step_pairs"].tolist() == OR.step_pairs_sequential_closed_form(S, cp)
+    assert plan["step_pairs"].sum(axis=1).tolist() == OR.sequential_split_pairs(S, cp)
+    if S <= 128:
+        assert plan["step_pairs"].tolist() == OR.step_pairs_enumerated(S, cp, "sequential")
+    balanced = cpa.cp_plan_chunks(S, cp, cpa.CP_LAYOUT_BALANCED)
+    assert balanced["step_pairs"].tolist() == cpa.cp_plan_balanced_chunks(S, cp)["step_pairs"].tolist()
+
+
+def test_plan_rejects_unknown_layout(cpa):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_plan_chunks(16, 2, 2)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("layout,r0,r1", [(2, 0, 1), (-1, 0, 1), (0, -1, 1), (0, 1, 1), (0, 0, 3), (1, 2, 1)])
+def test_rank_range_rejects(cpa, layout, r0, r1):
+    desc = cpa.make_desc(1, 1024, 4, 4, 64, 2, 0.125, 1)
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_rank_partial_attn(desc, layout, r0, r1, 0, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, stream=0)
+    assert e.value.status == 1
 
 
 @pytest.mark.parametrize("S,cp", [(0, 1), (10, 0), (10, -2), (10, 3), (7, 1), (12, 4)])

@@ -167,6 +167,69 @@ def test_invalid_arguments_launch_nothing():
     assert cpa.cp_take_device_status() == 0
 
 
+SEQ = cpa.CP_LAYOUT_SEQUENTIAL
+
+
+def _run_ranks(q, k, v, cp, layout, r0, r1, t0, t1, mode, bufs):
+    b, S, hq, d = q.shape
+    desc = cpa.make_desc(b, S, hq, k.shape[2], d, cp, 1.0 / math.sqrt(d), 1)
+    cpa.cp_ring_rank_partial_attn(desc, layout, r0, r1, t0, t1, q, k, v, *bufs, mode)
+    assert cpa.cp_take_device_status() == 0
+
+
+@pytest.mark.parametrize("case", [SMALL[0], SMALL[1], SMALL[3], SMALL[4], SMALL[7]],
+                         ids=["tiny", "b2", "ragged_g3", "cp8", "cp5"])
+def test_sequential_layout_full_ring_equals_causal_attention(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=31)
+    bufs = ring_buffers(b, S, hq, d)
+    _run_ranks(q, k, v, cp, SEQ, 0, cp, 0, cp, EMIT | FIN, bufs)
+    ref_out, ref_m, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(bufs[0].cpu().numpy(), ref_out, f"sequential {case}")
+    assert np.abs(bufs[1].cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+def test_sequential_layout_step_triples():
+    b, S, hq, hkv, d, cp, std = 1, 1024, 4, 2, 128, 4, 0.5
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=32)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    for t in range(cp):
+        bufs = ring_buffers(b, S, hq, d)
+        _run_ranks(q, k, v, cp, SEQ, 0, cp, t, t + 1, EMIT, bufs)
+        o, m, l = (x.cpu().numpy() for x in bufs)
+        for r in range(cp):
+            rows, rm, rl, ro = OR.ring_step_triple(qf, kf, vf, 1.0 / math.sqrt(d), cp, r, t, layout="sequential")
+            gm, gl, go = m[:, :, rows], l[:, :, rows], np.moveaxis(o[:, rows], 1, 2)
+            empty = np.isneginf(rm)
+            assert np.all(np.isneginf(gm[empty])) and np.all(gl[empty] == 0) and np.all(go[empty] == 0)
+            live = ~empty
+            if live.any():
+                assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
+                assert_out_close(go[live] / gl[live][:, None], ro[live] / rl[live][:, None], f"seq t{t} r{r}")
+
+
+@pytest.mark.parametrize("layout", [cpa.CP_LAYOUT_BALANCED, SEQ])
+def test_rank_ranges_touch_only_their_rows_and_compose(layout):
+    b, S, hq, hkv, d, cp = 1, 2048, 4, 2, 128, 4
+    q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=33)
+    full = ring_buffers(b, S, hq, d)
+    _run_ranks(q, k, v, cp, layout, 0, cp, 0, cp, EMIT | FIN, full)
+    lay = "sequential" if layout == SEQ else "balanced"
+    parts = ring_buffers(b, S, hq, d)
+    for x in parts:
+        x.fill_(float("nan"))
+    for r in range(cp):
+        _run_ranks(q, k, v, cp, layout, r, r + 1, 0, cp, EMIT | FIN, parts)
+        done = np.concatenate([OR.rank_rows(S, cp, rr, lay) for rr in range(r + 1)])
+        rest = np.setdiff1d(np.arange(S), done)
+        o = parts[0].cpu().numpy()
+        assert np.isnan(o[0, rest]).all(), "a rank launch wrote rows it does not own"
+        assert np.isfinite(o[0, done]).all()
+    # each rank's rows match the all-ranks launch bit for bit (same tiles, same order)
+    for x, y in zip(parts, full):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("name", ["gqa", "long"])
 def test_full_size_workload_sampled_rows(name):
     """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled."""

@@ -336,6 +336,26 @@ def test_pair_counts_enumeration_equals_closed_form(S, cp):
     assert totals[0] == C * (2 * cp * C + 1)
 
 
+@pytest.mark.parametrize("S,cp", [(8, 1), (16, 2), (24, 3), (64, 4), (96, 8)])
+def test_sequential_layout_pairs_and_totals(S, cp):
+    enum = OR.step_pairs_enumerated(S, cp, "sequential")
+    assert enum == OR.step_pairs_sequential_closed_form(S, cp)
+    assert [sum(row) for row in enum] == OR.sequential_split_pairs(S, cp)
+    assert sum(sum(row) for row in enum) == S * (S + 1) // 2
+    assert OR.rank_chunks(cp, "sequential") == [[2 * r, 2 * r + 1] for r in range(cp)]
+
+
+def test_sequential_layout_ring_equals_full_attention():
+    b, S, hq, hkv, d = 1, 48, 4, 2, 8
+    q, k, v = _rand((b, S, hq, d), 171), _rand((b, S, hkv, d), 172), _rand((b, S, hkv, d), 173)
+    _, m, l, onum = OA.full_causal_attention(q, k, v, 0.3)
+    for cp in (1, 2, 3, 4):
+        rm, rl, ro = OR.ring_attention(q, k, v, 0.3, cp, layout="sequential")
+        np.testing.assert_array_equal(rm, m)
+        np.testing.assert_allclose(rl, l, rtol=1e-13)
+        np.testing.assert_allclose(ro, onum, rtol=1e-12, atol=1e-13)
+
+
 def test_sequential_split_is_unbalanced():
     # the comparison the Terms table draws: a plain split loads the last rank far more
     S, cp = 4096, 8
