@@ -24,6 +24,7 @@ __all__ = [
     "cp_plan_balanced_chunks", "cp_plan_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn",
     "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
+    "cp_merge_tree_workspace_bytes", "cp_merge_partials_tree",
 ]
 
 CP_OK = 0
@@ -98,6 +99,9 @@ def load_library():
         "cp_passq_workspace_bytes": (_I32, [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]),
         "cp_passq_decode": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P]),
         "cp_take_device_status": (_I32, [_P, ctypes.POINTER(_I32)]),
+        "cp_merge_tree_workspace_bytes": (_I32, [_I64, _I64, _I64, _I64, _I32, ctypes.POINTER(ctypes.c_size_t)]),
+        "cp_merge_partials_tree": (_I32, [_I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P,
+                                          _I32, _P]),
         "cp_passq_decode_noalloc": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -210,6 +214,24 @@ def cp_merge_partials(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts,
                                _ptr(m_parts), _ptr(l_parts), order_ptr, _ptr(o_out), _ptr(m_out), _ptr(l_out),
                                int(bool(finalize)), _stream(stream))
     _check(st, "cp_merge_partials")
+
+
+def cp_merge_tree_workspace_bytes(batch, rows, heads, d, n_parts) -> int:
+    lib = load_library()
+    n = ctypes.c_size_t(0)
+    _check(lib.cp_merge_tree_workspace_bytes(int(batch), int(rows), int(heads), int(d), int(n_parts),
+                                             ctypes.byref(n)), "cp_merge_tree_workspace_bytes")
+    return int(n.value)
+
+
+def cp_merge_partials_tree(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, workspace, workspace_bytes,
+                           o_out, m_out, l_out, finalize=False, stream=None) -> None:
+    """Log-depth tree reduction of n_parts (a power of two) triples; part i merges with part i + n/2."""
+    lib = load_library()
+    st = lib.cp_merge_partials_tree(int(batch), int(rows), int(heads), int(d), int(n_parts), _ptr(o_parts),
+                                    _ptr(m_parts), _ptr(l_parts), _ptr(workspace), int(workspace_bytes), _ptr(o_out),
+                                    _ptr(m_out), _ptr(l_out), int(bool(finalize)), _stream(stream))
+    _check(st, "cp_merge_partials_tree")
 
 
 def cp_passq_workspace_bytes(desc: AttnDesc) -> int:

@@ -171,6 +171,28 @@ CPATTN_API cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t head
                             void* cuda_stream);
 
 /*
+ * Tree-structured reduction of n_parts triples (n_parts a power of two >= 2), the
+ * O(log cp)-depth reduce topology the spec lists as later work (Limitations
+ * table, "pass-Q 归约拓扑固定": Tree Attention's log-depth steps).  Level k merges
+ * part i with part i + n/2 for every i, halving n, until one triple is left; each
+ * level is one launch of the LSE merge kernel.  The result equals
+ * cp_merge_partials up to rounding (the merge is associative).  Same layouts as
+ * cp_merge_partials; `workspace` (device, caller-owned) holds two ping-pong levels
+ * of n_parts/2 triples: cp_merge_tree_workspace_bytes gives its size.  Inputs are
+ * not modified.
+ * Errors: n_parts not a power of two >= 2, sizes < 1, d % 4 != 0, a NULL or
+ * misaligned pointer, a workspace below the required size ->
+ * CP_ERR_INVALID_ARGUMENT; d > 512 -> CP_ERR_UNSUPPORTED.
+ */
+CPATTN_API cp_status cp_merge_tree_workspace_bytes(int64_t batch, int64_t rows, int64_t heads, int64_t d,
+                                                   int32_t n_parts, size_t* bytes);
+CPATTN_API cp_status cp_merge_partials_tree(int64_t batch, int64_t rows, int64_t heads, int64_t d,
+                                            int32_t n_parts, const float* o_parts, const float* m_parts,
+                                            const float* l_parts, float* workspace, size_t workspace_bytes,
+                                            float* o_out, float* m_out, float* l_out, int32_t finalize,
+                                            void* cuda_stream);
+
+/*
  * Bytes of device workspace cp_passq_decode needs for `desc` on the CURRENT
  * device (the split count depends on its SM count).  Host-only.
  * Errors: as cp_passq_decode's argument checks.

@@ -171,6 +171,17 @@ def merge_tree(parts):
     return level[0]
 
 
+def merge_tree_halves(parts):
+    """Log-depth tree where each level merges part i with part i + n/2 (n a power of two)."""
+    level = list(parts)
+    if len(level) & (len(level) - 1):
+        raise ValueError("the halving tree needs a power-of-two number of parts")
+    while len(level) > 1:
+        half = len(level) // 2
+        level = [merge(level[i], level[i + half]) for i in range(half)]
+    return level[0]
+
+
 def finalize(triple):
     """Normalised output O / l (0 where l = 0) and lse = m + ln l."""
     m, l, o = triple

@@ -35,7 +35,8 @@ def _declared_symbols():
 def test_header_declares_the_boundary():
     syms = _declared_symbols()
     for name in ["cp_plan_balanced_chunks", "cp_plan_chunks", "cp_ring_step_partial_attn",
-                 "cp_ring_rank_partial_attn", "cp_merge_partials", "cp_passq_decode", "cp_comm_bytes",
+                 "cp_ring_rank_partial_attn", "cp_merge_partials", "cp_merge_partials_tree",
+                 "cp_merge_tree_workspace_bytes", "cp_passq_decode", "cp_comm_bytes",
                  "cp_passq_workspace_bytes", "cp_status_string", "cp_take_device_status"]:
         assert name in syms, name
 
@@ -248,3 +249,15 @@ def test_binding_has_no_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(cpa, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         cpa.cp_comm_bytes(8, 2, 1)
+
+
+@pytest.mark.parametrize("n", [0, 1, 3, 6, 12])
+def test_tree_merge_needs_a_power_of_two(cpa, n):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, n)
+    assert e.value.status == 1
+
+
+def test_tree_merge_workspace_size(cpa):
+    # two ping-pong levels of n/2 triples: O (d floats) + m + l per (part, batch, row, head)
+    assert cpa.cp_merge_tree_workspace_bytes(1, 4096, 64, 128, 32) == 2 * 16 * 4096 * 64 * (128 + 2) * 4

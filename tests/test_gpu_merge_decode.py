@@ -127,6 +127,55 @@ def test_merge_stress_workload_orders_and_tree():
     assert np.abs(ref_l[0][hs].T.cpu().double().numpy() - rl).max() <= MERGE_REL * np.abs(rl).max()
 
 
+def _merge_tree(o, m, l, finalize=False):
+    n, b, rows, heads, d = o.shape
+    nbytes = cpa.cp_merge_tree_workspace_bytes(b, rows, heads, d, n)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=o.device)
+    oo = torch.empty((b, rows, heads, d), dtype=torch.float32, device=o.device)
+    mo = torch.empty((b, heads, rows), dtype=torch.float32, device=o.device)
+    lo = torch.empty_like(mo)
+    cpa.cp_merge_partials_tree(b, rows, heads, d, n, o, m, l, ws, nbytes, oo, mo, lo, finalize=finalize)
+    return oo, mo, lo
+
+
+@pytest.mark.parametrize("shape", [(2, 1, 37, 3, 8), (4, 2, 33, 2, 64), (8, 1, 96, 5, 128), (32, 1, 64, 4, 128),
+                                   (256, 1, 16, 2, 16), (16, 3, 1, 16, 512)])
+def test_tree_merge_matches_oracle_and_flat_merge(shape):
+    n, b, rows, heads, d = shape
+    draws = [synth.merge_parts(n, heads, rows, d, spread=80.0, seed=7 * n + d + bi) for bi in range(b)]
+    o = torch.cat([x[0] for x in draws], dim=1).contiguous()
+    m = torch.cat([x[1] for x in draws], dim=1).contiguous()
+    l = torch.cat([x[2] for x in draws], dim=1).contiguous()
+    for fin in (False, True):
+        to, tm, tl = _merge_tree(o, m, l, finalize=fin)
+        fo, fm, fl = _merge(o, m, l, finalize=fin)
+        torch.cuda.synchronize()
+        assert torch.equal(tm, fm)  # max is exact in any grouping
+        assert ((tl - fl).abs() <= MERGE_REL * fl.abs()).all()
+        assert_rowwise_rel(to.cpu().numpy(), fo.cpu().numpy().astype(np.float64), MERGE_REL, f"tree vs flat {shape}")
+        for bi in range(b):
+            parts = [(m[p, bi].T.cpu().double().numpy(), l[p, bi].T.cpu().double().numpy(),
+                      o[p, bi].cpu().double().numpy()) for p in range(n)]
+            rm, rl, ro = OR.merge_tree_halves(parts)
+            assert np.array_equal(tm[bi].T.cpu().double().numpy(), rm)
+            ref = OR.finalize((rm, rl, ro))[0] if fin else ro
+            assert_rowwise_rel(to[bi].cpu().numpy(), ref, MERGE_REL, f"tree vs oracle {shape}")
+
+
+def test_tree_merge_rejects_bad_part_counts():
+    o, m, l = synth.merge_parts(3, 2, 8, 8, seed=1)
+    with pytest.raises(cpa.CpError):
+        cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, 3)
+    ws = torch.empty(1 << 16, dtype=torch.float32, device="cuda")
+    out = torch.empty((1, 8, 2, 8), dtype=torch.float32, device="cuda")
+    ml = torch.empty((1, 2, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(cpa.CpError):
+        cpa.cp_merge_partials_tree(1, 8, 2, 8, 3, o, m, l, ws, ws.numel() * 4, out, ml, ml.clone())
+    need = cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, 2)
+    with pytest.raises(cpa.CpError):
+        cpa.cp_merge_partials_tree(1, 8, 2, 8, 2, o[:2], m[:2], l[:2], ws, need - 4, out, ml, ml.clone())
+
+
 # ------------------------------------------------------------------ decode
 
 def _decode(q, k, v, cp):

@@ -516,3 +516,16 @@ def test_pins_catch_planted_attention_mistakes(kind):
 @pytest.mark.parametrize("kind", ["sign", "drop_b_in_l", "no_guard"])
 def test_pins_catch_planted_merge_mistakes(kind):
     assert _fails(check_merge, _mutant_merge(kind)), f"planted merge mistake {kind!r} slipped through"
+
+
+def test_halving_tree_equals_fold_and_pairwise_tree():
+    parts = _random_triples(16, 120, 6, 181, spread=40.0, identity_frac=0.02)
+    parts[0][0][:] = np.where(np.isneginf(parts[0][0]), 0.0, parts[0][0])
+    parts[0][1][:] = np.where(parts[0][1] == 0, 1.0, parts[0][1])
+    fold = OR.merge_in_order(parts)
+    for tree in (OR.merge_tree_halves(parts), OR.merge_tree(parts)):
+        np.testing.assert_array_equal(tree[0], fold[0])
+        np.testing.assert_allclose(tree[1], fold[1], rtol=1e-13)
+        np.testing.assert_allclose(tree[2], fold[2], rtol=1e-12, atol=1e-300)
+    with pytest.raises(ValueError):
+        OR.merge_tree_halves(parts[:3])
