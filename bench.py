@@ -463,6 +463,26 @@ def secondary_lines(cpa, synth, peaks, stream):
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": 2}
     del q, k, v, ws
     torch.cuda.empty_cache()
+    # pass-Q decode with 16 query heads sharing one 512-wide K/V head (MQA / MLA-style), tensor cores
+    b, L, hq, hkv, d, cp = 8, 131072, 16, 1, 512, 8
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=20260006)
+    desc = cpa.make_desc(b, L, hq, hkv, d, cp, 1.0 / math.sqrt(d), 0)
+    nbytes = cpa.cp_passq_workspace_bytes(desc)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    res = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    fn = lambda: cpa.cp_passq_decode(desc, q, k, v, ws, nbytes, res, None, None, stream)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 20, stream)
+    wd = dict(b=b, S=L, h_q=hq, h_kv=hkv, d=d, cp=cp)
+    gbs = decode_bytes(wd) / (ms * 1e-3) / 1e9
+    out["decode_shared_kv"] = {"workload": "pass-Q decode, 16 q heads on one 512-wide K/V head: b8, L131072, cp8",
+                               "value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4), "bytes": decode_bytes(wd),
+                               "tflops": round(4 * b * hq * d * L / (ms * 1e-3) / 1e12, 1),
+                               "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+                               "kernel": "mqa_decode_kernel<512,16> (tcgen05) + lse merge"}
+    del q, k, v, ws
+    torch.cuda.empty_cache()
     # LSE merge: 32 parts x 64 heads x 4096 rows x 128
     w = synth.WORKLOADS["merge"]
     po, pm, pl = synth.merge_parts(w["parts"], w["heads"], w["rows"], w["d"], spread=w["spread"], seed=w["seed"])

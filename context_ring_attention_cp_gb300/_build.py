@@ -1,6 +1,6 @@
 """Builds ``libcpattn.so`` in-tree with nvcc for sm_103a.
 
-The four translation units compile in parallel (one ``-gencode``), then link
+The translation units compile in parallel (one ``-gencode``), then link
 into a shared library beside this file.  Nothing is installed anywhere else.
 """
 
@@ -15,8 +15,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcpattn.so")
-SOURCES = ["capi.cpp", "merge.cu", "decode.cu", "ring_attn.cu"]
-HEADERS = ["internal.h", os.path.join("..", "..", "include", "cpattn.h")]
+SOURCES = ["capi.cpp", "merge.cu", "decode.cu", "decode_mqa.cu", "ring_attn.cu"]
+HEADERS = ["internal.h", "tc_ptx.h", os.path.join("..", "..", "include", "cpattn.h")]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

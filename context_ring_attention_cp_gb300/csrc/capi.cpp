@@ -374,9 +374,9 @@ cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const
 cp_status cp_take_device_status(void* cuda_stream, int32_t* status) {
   if (status == nullptr) return CP_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CP_ERR_CUDA;
-  int32_t s = CP_OK;
-  if (ring_take_status(&s) != cudaSuccess) return CP_ERR_CUDA;
-  *status = s;
+  int32_t s = CP_OK, s2 = CP_OK;
+  if (ring_take_status(&s) != cudaSuccess || mqa_take_status(&s2) != cudaSuccess) return CP_ERR_CUDA;
+  *status = (s != CP_OK) ? s : s2;
   return CP_OK;
 }
 

@@ -237,17 +237,25 @@ __global__ void __launch_bounds__(kThreads) passq_partial_kernel(const __grid_co
 
 }  // namespace
 
-bool decode_supported(const cp_attn_desc& d) {
+namespace {
+// The streaming SIMT kernel of this file: small query groups.
+bool simt_supported(const cp_attn_desc& d) {
   const int64_t g = d.h_q / d.h_kv;
   const bool dim_ok = d.d == 64 || d.d == 128 || d.d == 256 || d.d == 512;
   // Shared memory holds kWarps x g x d floats of per-warp partials: g * d <= 1024.
   return dim_ok && (g == 1 || g == 2 || g == 4) && g * d.d <= 1024;
 }
+}  // namespace
+
+// g in {1, 2, 4}: the SIMT streaming kernel below; g in {16, 32} (heads sharing
+// one K/V head): the tensor-core kernel of decode_mqa.cu.
+bool decode_supported(const cp_attn_desc& d) { return simt_supported(d) || decode_mqa_supported(d); }
 
 // Cut every shard into `splits` ranges so that about eight CTAs per SM are
 // launched in total (a whole number of waves matters less than a short tail).
 // `splits` divides the shard length; parts stay within CP_MAX_MERGE_PARTS.
 int32_t decode_splits_per_shard(const cp_attn_desc& d, int sm_count) {
+  if (!simt_supported(d)) return decode_mqa_splits(d, sm_count);
   const int64_t shard = d.S / d.cp;
   const int64_t groups = d.b * d.h_kv * d.cp;
   const int64_t target = int64_t(sm_count > 0 ? sm_count : 148) * 8;
@@ -278,6 +286,7 @@ void decode_workspace_sections(const cp_attn_desc& d, int32_t splits, float* ws,
 cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const void* q,
                                    const void* k, const void* v, float* o_parts,
                                    float* m_parts, float* l_parts, cudaStream_t stream) {
+  if (!simt_supported(d)) return launch_decode_mqa(d, splits, q, k, v, o_parts, m_parts, l_parts, stream);
   DecodeParams p;
   p.q = static_cast<const uint16_t*>(q);
   p.k = static_cast<const uint16_t*>(k);

@@ -1,0 +1,513 @@
+// Pass-Q decode for query heads that share one K/V head (MQA / MLA-style), on
+// sm_103a tensor cores.
+//
+// "G5 上下文并行建模设计规格": Terms table row "Pass-Q" (query to every rank,
+// local partial attention per KV shard, then the reduce), c_kv row (for MLA the
+// compressed per-token K/V), use-case decode paragraph.  With g = h_q / h_kv
+// query heads on one K/V head (g = 16 x 512 on the pypto-lib issue page's per-card
+// shapes), every K/V byte feeds 16 dot products: at HBM speed that is ~16 FLOP/B,
+// beyond the FP32 pipes, so both contractions run on tcgen05.
+//
+// Transposed formulation, one CTA per (KV range, sequence, kv head):
+//   S^T = K Q^T   M = 128 keys, N = g heads, K = d      (A = K tile, B = Q, both K-major)
+//   O^T += V^T P^T  M = 128-wide d block, N = g, K = 128 keys
+//                   (A = V tile read MN-major, B = P^T written by the softmax warps)
+// so g = 16 heads fill an N = 16 instruction with no padding.  K and V stream
+// through a ring of 16 KB slots (128 keys x 64 d, 128-byte swizzle), loaded in
+// exactly the order the MMAs consume them: K_0, then (K_{j+1}, V_j) per tile.
+// A tile's V slabs come in groups of d/64 >= 2 starting on an even slot of an
+// even-sized ring, so the two 64-wide halves of a d block sit in adjacent slots
+// and the MN-major descriptor's leading offset is one slot.
+//
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer (one lane), 4-7 softmax and
+// epilogue (thread = key lane of S^T, and = d lane of O^T).  Per-head maxima over
+// the 128 keys of a tile come from a warp butterfly plus a shared-memory reduction
+// across the four warps; the exponent reference is raised only when a head's max
+// grows by more than 8 (log2 units), O^T columns are then rescaled in TMEM.  Row
+// sums stay per thread until the epilogue.  The CTA writes its partial triple per
+// query head to the decode workspace, which the LSE merge kernel reduces.
+//
+// Every mbarrier wait is bounded (tc_ptx.h); on expiry CP_ERR_TIMEOUT goes to this
+// file's status word and the CTA returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+#include "tc_ptx.h"
+
+namespace cpattn {
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 128;        // keys per tile (M of S^T)
+constexpr int kSlabBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ int32_t g_mqa_status = 0;
+
+template <int D, int G>
+struct MqaCfg {
+  static constexpr int kSlabsPerTile = D / 64;      // K or V slabs per 128-key tile
+  static constexpr int kQSlab = G * 128;            // bytes of one Q slab (G rows x 64 d)
+  static constexpr int kQBytes = kSlabsPerTile * kQSlab;
+  static constexpr int kPSlab = G * 128;            // bytes of one P^T slab (G rows x 64 keys)
+  static constexpr int kPBytes = 2 * kPSlab;        // one P^T buffer (128 keys)
+  static constexpr int kSlots = (G == 16) ? 12 : 10;  // even ring size
+  static constexpr int kQOff = 0;
+  static constexpr int kPOff = kQBytes;             // two P^T buffers
+  static constexpr int kRingOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * kSlabBytes;
+  static constexpr int kRedOff = kBarOff + 512;     // [2][4][G] per-warp maxima, then [4][G] row sums
+  static constexpr int kSmemBytes = kRedOff + 3 * 4 * G * 4 + 1024;
+  static constexpr uint32_t kOCol = 2 * G;          // S^T buffers at [0, G) and [G, 2G)
+  static constexpr uint32_t kTmemCols = (2 * G + (D / 128) * G) <= 64 ? 64 : ((2 * G + (D / 128) * G) <= 128 ? 128 : 256);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSlots % 2 == 0, "V slab pairs must not wrap the ring");
+  static_assert(kQSlab % 1024 == 0 && kPSlab % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+};
+
+struct MqaParams {
+  CUtensorMap tmap_q;  // dims (d, h_q, b), box (64, G, 1)
+  CUtensorMap tmap_k;  // dims (d, h_kv, L, b), box (64, 1, 128, 1)
+  CUtensorMap tmap_v;
+  float* o_parts;  // [n_parts, b, h_q, d]
+  float* m_parts;  // [n_parts, b, h_q]
+  float* l_parts;
+  int64_t b, L, h_q, h_kv;
+  int64_t part_len;
+  int32_t n_parts;
+  float sl;  // scale * log2(e)
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_constant__ MqaParams p) {
+  using K = MqaCfg<D, G>;
+  constexpr int NS = K::kSlabsPerTile;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::kBarOff);
+  const uint32_t bar_q = smem_u32(&bars[0]);
+  auto bar_full = [&](int s) { return smem_u32(&bars[1 + s]); };
+  auto bar_empty = [&](int s) { return smem_u32(&bars[1 + K::kSlots + s]); };
+  auto bar_s = [&](int b) { return smem_u32(&bars[1 + 2 * K::kSlots + b]); };
+  auto bar_p = [&](int b) { return smem_u32(&bars[3 + 2 * K::kSlots + b]); };
+  const uint32_t bar_o = smem_u32(&bars[5 + 2 * K::kSlots]);
+  const uint32_t bar_red = smem_u32(&bars[6 + 2 * K::kSlots]);  // the four softmax warps, one phase per tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[7 + 2 * K::kSlots]);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(smem + K::kRedOff);  // [2][4][G] maxima
+  float* red_l = red + 2 * 4 * G;                             // [4][G] row sums
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int part = blockIdx.x;
+  const int64_t bk = blockIdx.y;  // sequence * h_kv + kv head
+  const int32_t kvh = int32_t(bk % p.h_kv);
+  const int32_t bi = int32_t(bk / p.h_kv);
+  const int64_t k_begin = int64_t(part) * p.part_len;
+  const int64_t k_end = k_begin + p.part_len;
+  const int32_t n_tiles = int32_t((p.part_len + BK - 1) / BK);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < K::kSlots; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_s(b), 1);
+      mbar_init(bar_p(b), 4);
+    }
+    mbar_init(bar_o, 1);
+    mbar_init(bar_red, 4);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_mqa_status) != 0) ? 1 : 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(K::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+  auto wait = [&](uint32_t bar, uint32_t parity) { return mbar_wait_bounded(bar, parity, abort_flag, &g_mqa_status); };
+
+  if (skip) {
+    // an earlier wait gave up: nothing to do
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(bar_q, uint32_t(K::kQBytes));
+      for (int sl = 0; sl < NS; ++sl)
+        tma_load_3d(sbase + K::kQOff + sl * K::kQSlab, &p.tmap_q, bar_q, sl * 64, kvh * G, bi);
+      int32_t li = 0;  // running load index, in MMA consumption order
+      bool ok = true;
+      auto load_tile = [&](const CUtensorMap* map, int32_t tile) {
+        const int32_t key0 = int32_t(k_begin) + tile * BK;
+        for (int sl = 0; sl < NS && ok; ++sl, ++li) {
+          const int s = li % K::kSlots, round = li / K::kSlots;
+          if (round > 0 && !wait(bar_empty(s), uint32_t((round - 1) & 1))) { ok = false; break; }
+          mbar_expect_tx(bar_full(s), uint32_t(kSlabBytes));
+          tma_load_4d(sbase + K::kRingOff + s * kSlabBytes, map, bar_full(s), sl * 64, kvh, key0, bi);
+        }
+      };
+      load_tile(&p.tmap_k, 0);
+      for (int32_t j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) load_tile(&p.tmap_k, j + 1);
+        if (ok) load_tile(&p.tmap_v, j);
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = instr_desc_bf16(128, G, false, false);
+      constexpr uint32_t idesc_o = instr_desc_bf16(128, G, true, false);
+      int32_t li = 0;
+      bool ok = wait(bar_q, 0);
+      // S^T(j) into S buffer j % 2 from the K slabs of tile j (next NS slots in order)
+      auto issue_s = [&](int32_t j) {
+        const uint32_t d_tm = tmem + uint32_t(j & 1) * G;
+        for (int sl = 0; sl < NS && ok; ++sl, ++li) {
+          const int s = li % K::kSlots;
+          if (!wait(bar_full(s), uint32_t((li / K::kSlots) & 1))) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ka = sbase + K::kRingOff + s * kSlabBytes;
+          const uint32_t qa = sbase + K::kQOff + sl * K::kQSlab;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // 16 d per k-step = 32 bytes into the 128-byte row
+            mma_ss(d_tm, smem_desc(ka + kk * 32, 16, 1024), smem_desc(qa + kk * 32, 16, 1024), idesc_s,
+                   (sl > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty(s));
+        }
+      };
+      // O^T += V^T(j) P^T(j): d blocks of 128 = slab pairs, 8 k-steps of 16 keys each
+      auto issue_o = [&](int32_t j) {
+        const uint32_t pa = sbase + K::kPOff + uint32_t(j & 1) * K::kPBytes;
+        for (int blk = 0; blk < NS / 2 && ok; ++blk, li += 2) {
+          const int s0 = li % K::kSlots, s1 = (li + 1) % K::kSlots;
+          if (!wait(bar_full(s0), uint32_t((li / K::kSlots) & 1)) ||
+              !wait(bar_full(s1), uint32_t(((li + 1) / K::kSlots) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t va = sbase + K::kRingOff + s0 * kSlabBytes;  // s1 == s0 + 1 (even slot, even ring)
+          const uint32_t d_tm = tmem + K::kOCol + uint32_t(blk) * G;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ss(d_tm, smem_desc(va + kk * 2048, kSlabBytes, 1024),
+                   smem_desc(pa + (kk / 4) * K::kPSlab + (kk % 4) * 32, 16, 1024), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty(s0));
+          mma_commit(bar_empty(s1));
+        }
+      };
+      if (ok) {
+        issue_s(0);
+        if (ok) mma_commit(bar_s(0));
+      }
+      for (int32_t j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) {
+          issue_s(j + 1);
+          if (!ok) break;
+          mma_commit(bar_s((j + 1) & 1));
+        }
+        if (!wait(bar_p(j & 1), uint32_t((j >> 1) & 1))) { ok = false; break; }
+        tc_fence_after();
+        issue_o(j);
+        if (!ok) break;
+        mma_commit(bar_o);
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 50000ull) {
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = threadIdx.x - 128;  // key lane of S^T, d lane of O^T
+    const int wq = warp - 4;
+    const uint32_t lane_base = uint32_t(wq * 32) << 16;
+    float m_ref[G], m_true[G], l_t[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m_ref[h] = -INFINITY;
+      m_true[h] = -INFINITY;
+      l_t[h] = 0.f;
+    }
+    bool ok = true;
+    for (int32_t j = 0; j < n_tiles; ++j) {
+      if (!__all_sync(0xffffffffu, wait(bar_s(j & 1), uint32_t((j >> 1) & 1)))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[G];
+      if constexpr (G == 16) {
+        tmem_ld16(tmem + lane_base + uint32_t(j & 1) * G, sr);
+        tmem_ld_wait16(sr);
+      } else {
+        tmem_ld32(tmem + lane_base + uint32_t(j & 1) * G, sr);
+        tmem_ld_wait(sr);
+      }
+      const int64_t key = k_begin + int64_t(j) * BK + t;
+      const bool valid = key < k_end;
+      float x[G], mx[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        x[h] = valid ? __uint_as_float(sr[h]) : -INFINITY;
+        mx[h] = x[h];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+      }
+      // Cross-warp maxima through shared memory, double-buffered by tile parity; the
+      // barrier is an mbarrier (bounded wait), not bar.sync, so a warp that gave up
+      // cannot leave the others waiting forever.
+      float* rb = red + (j & 1) * 4 * G;
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) rb[wq * G + h] = mx[h];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_red);
+      if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(j & 1)))) { ok = false; break; }
+      bool any_raise = false;
+      float f[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float tmax = fmaxf(fmaxf(rb[h], rb[G + h]), fmaxf(rb[2 * G + h], rb[3 * G + h])) * p.sl;
+        m_true[h] = fmaxf(m_true[h], tmax);
+        const bool raise = tmax > m_ref[h] + kRescaleThreshold;
+        f[h] = 1.f;
+        if (raise) {
+          f[h] = (m_ref[h] == -INFINITY) ? 0.f : ex2(m_ref[h] - tmax);
+          any_raise = any_raise || (j > 0 && m_ref[h] != -INFINITY);
+          l_t[h] *= f[h];
+          m_ref[h] = tmax;
+        }
+      }
+      // O^T(j-1) complete before it is rescaled and before P buffer j%2 (read by O^T(j-2)) is rewritten
+      if (j > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((j - 1) & 1)))) { ok = false; break; }
+      tc_fence_after();
+      if (any_raise) {  // identical in every thread: decided from the shared maxima
+#pragma unroll
+        for (int blk = 0; blk < D / 128; ++blk) {
+          const uint32_t oaddr = tmem + lane_base + K::kOCol + uint32_t(blk) * G;
+          uint32_t r[G];
+          if constexpr (G == 16) {
+            tmem_ld16(oaddr, r);
+            tmem_ld_wait16(r);
+#pragma unroll
+            for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
+            tmem_st16(oaddr, r);
+          } else {
+            tmem_ld32(oaddr, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
+            tmem_st32(oaddr, r);
+          }
+        }
+        tmem_st_wait();
+      }
+      // P^T(j): row h, key column t of a [G x 128] K-major, 128-byte-swizzled operand
+      uint8_t* pbuf = smem + K::kPOff + (j & 1) * K::kPBytes + (t / 64) * K::kPSlab;
+      const int c16 = (t % 64) / 8, within = (t % 8) * 2;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pv = ex2(fmaf(x[h], p.sl, -((m_ref[h] == -INFINITY) ? 0.f : m_ref[h])));
+        l_t[h] += pv;
+        const __nv_bfloat16 bv = __float2bfloat16_rn(pv);
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + h * 128 + ((c16 ^ (h % 8)) << 4) + within) = bv;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(j & 1));
+    }
+
+    // ---------------- epilogue: this range's partial triple per query head
+    if (ok && n_tiles > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((n_tiles - 1) & 1)))) ok = false;
+    if (ok) {
+      tc_fence_after();
+      // row sums over the 128 key lanes: butterfly, then the four warps
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) l_t[h] += __shfl_xor_sync(0xffffffffu, l_t[h], off);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) red_l[wq * G + h] = l_t[h];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_red);
+      if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(n_tiles & 1)))) ok = false;
+    }
+    if (ok) {
+      const int64_t row0 = (int64_t(part) * p.b + bi) * p.h_q + int64_t(kvh) * G;
+#pragma unroll
+      for (int blk = 0; blk < D / 128; ++blk) {
+        uint32_t r[G];
+        const uint32_t oaddr = tmem + lane_base + K::kOCol + uint32_t(blk) * G;
+        if constexpr (G == 16) {
+          tmem_ld16(oaddr, r);
+          tmem_ld_wait16(r);
+        } else {
+          tmem_ld32(oaddr, r);
+          tmem_ld_wait(r);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          // re-express against the true max: factor 2^(m_ref - m_true) <= 1
+          const float fre = (m_true[h] == -INFINITY) ? 0.f : ex2(m_ref[h] - m_true[h]);
+          p.o_parts[(row0 + h) * D + blk * 128 + t] = __uint_as_float(r[h]) * fre;
+        }
+      }
+      if (t < G) {
+        float lsum = 0.f, mt = 0.f, mr = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (h == t) {
+            mt = m_true[h];
+            mr = m_ref[h];
+          }
+        }
+        lsum = red_l[t] + red_l[G + t] + red_l[2 * G + t] + red_l[3 * G + t];
+        const float fre = (mt == -INFINITY) ? 0.f : ex2(mr - mt);
+        p.m_parts[row0 + t] = mt * kLn2;  // natural-log units
+        p.l_parts[row0 + t] = lsum * fre;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(K::kTmemCols));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) !=
+            cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const MqaParams& p, dim3 grid, cudaStream_t stream) {
+  using K = MqaCfg<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(mqa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       K::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  mqa_decode_kernel<D, G><<<grid, kThreads, K::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_mqa_supported(const cp_attn_desc& d) {
+  const int64_t g = d.h_q / d.h_kv;
+  return (g == 16 || g == 32) && (d.d == 128 || d.d == 256 || d.d == 512) && d.S < (int64_t(1) << 31) &&
+         d.b <= 65535 && d.h_kv <= 65535;
+}
+
+// Ranges of at least 512 keys, about four waves of one CTA per SM.
+int32_t decode_mqa_splits(const cp_attn_desc& d, int sm_count) {
+  const int64_t shard = d.S / d.cp;
+  const int64_t groups = d.b * d.h_kv * d.cp;
+  const int64_t target = int64_t(sm_count > 0 ? sm_count : 148) * 4;
+  int64_t splits = 1;
+  while (groups * splits < target && shard % (splits * 2) == 0 && shard / (splits * 2) >= 512 &&
+         d.cp * splits * 2 <= CP_MAX_MERGE_PARTS)
+    splits *= 2;
+  return int32_t(splits);
+}
+
+cudaError_t launch_decode_mqa(const cp_attn_desc& d, int32_t splits, const void* q, const void* k, const void* v,
+                              float* o_parts, float* m_parts, float* l_parts, cudaStream_t stream) {
+  MqaParams p;
+  memset(&p, 0, sizeof(p));
+  const int G = int(d.h_q / d.h_kv);
+  {
+    const cuuint64_t dims[3] = {cuuint64_t(d.d), cuuint64_t(d.h_q), cuuint64_t(d.b)};
+    const cuuint64_t strides[2] = {cuuint64_t(d.d * 2), cuuint64_t(d.h_q * d.d * 2)};
+    const cuuint32_t box[3] = {64, cuuint32_t(G), 1};
+    if (!encode(&p.tmap_q, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {cuuint64_t(d.d), cuuint64_t(d.h_kv), cuuint64_t(d.S), cuuint64_t(d.b)};
+    const cuuint64_t strides[3] = {cuuint64_t(d.d * 2), cuuint64_t(d.h_kv * d.d * 2),
+                                   cuuint64_t(d.S * d.h_kv * d.d * 2)};
+    const cuuint32_t box[4] = {64, 1, BK, 1};
+    if (!encode(&p.tmap_k, k, 4, dims, strides, box) || !encode(&p.tmap_v, v, 4, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  p.o_parts = o_parts;
+  p.m_parts = m_parts;
+  p.l_parts = l_parts;
+  p.b = d.b;
+  p.L = d.S;
+  p.h_q = d.h_q;
+  p.h_kv = d.h_kv;
+  p.n_parts = int32_t(d.cp * splits);
+  p.part_len = d.S / p.n_parts;
+  p.sl = d.scale * kLog2e;
+  const dim3 grid(unsigned(p.n_parts), unsigned(d.b * d.h_kv));
+#define CP_MQA(DD, GG) \
+  if (d.d == DD && G == GG) return launch_dg<DD, GG>(p, grid, stream);
+  CP_MQA(128, 16) CP_MQA(256, 16) CP_MQA(512, 16)
+  CP_MQA(128, 32) CP_MQA(256, 32) CP_MQA(512, 32)
+#undef CP_MQA
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t mqa_take_status(int32_t* status) {
+  int32_t s = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&s, g_mqa_status, sizeof(s));
+  if (e != cudaSuccess) return e;
+  const int32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_mqa_status, &zero, sizeof(zero));
+  *status = s;
+  return e;
+}
+
+}  // namespace cpattn

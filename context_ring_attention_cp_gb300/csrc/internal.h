@@ -42,6 +42,13 @@ cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const 
 size_t decode_noalloc_scratch_bytes();
 cudaError_t decode_noalloc_scratch(float** ptr);
 
+// ---- pass-Q decode for heads sharing one K/V head, tensor cores (decode_mqa.cu)
+bool decode_mqa_supported(const cp_attn_desc& d);
+int32_t decode_mqa_splits(const cp_attn_desc& d, int sm_count);
+cudaError_t launch_decode_mqa(const cp_attn_desc& d, int32_t splits, const void* q, const void* k, const void* v,
+                              float* o_parts, float* m_parts, float* l_parts, cudaStream_t stream);
+cudaError_t mqa_take_status(int32_t* status);
+
 // ---- ring-step attention (ring_attn.cu) ------------------------------------
 bool ring_supported(const cp_attn_desc& d);
 // Returns CP_OK, or CP_ERR_CUDA when a tensor map cannot be encoded or the launch fails.

@@ -210,8 +210,11 @@ CPATTN_API cp_status cp_passq_workspace_bytes(const cp_attn_desc* desc, size_t* 
  *   out   [b, h_q, d] fp32 = O / l,   m_out, l_out [b, h_q] fp32 (each nullable).
  * q [b, h_q, d] bf16; k, v [b, L, h_kv, d] bf16.  The query dispatch of the spec
  * is the shared q buffer.
- * Supported: d in {64, 128, 256, 512}; h_q / h_kv in {1, 2, 4} with
- * (h_q / h_kv) * d <= 1024; cp * splits <= CP_MAX_MERGE_PARTS; causal = 0.
+ * Supported: g = h_q / h_kv in {1, 2, 4} with d in {64, 128, 256, 512} and
+ * g * d <= 1024 (a streaming kernel on the FP32 pipes); or g in {16, 32} with d in
+ * {128, 256, 512} (query heads sharing one K/V head, MQA / MLA-style: both
+ * contractions on the tensor cores; k and v may be the same buffer);
+ * cp * splits <= CP_MAX_MERGE_PARTS; causal = 0.
  * Errors: cp < 1, L % cp != 0, sizes < 1, h_q % h_kv != 0, scale <= 0, NULL or
  * misaligned pointer, workspace_bytes below cp_passq_workspace_bytes ->
  * CP_ERR_INVALID_ARGUMENT; unsupported d, group or causal -> CP_ERR_UNSUPPORTED.

@@ -209,6 +209,58 @@ def test_decode_matches_oracle(case):
     assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
 
 
+# Query heads sharing one K/V head (MQA / MLA-style): the tensor-core decode kernel.
+MQA_SMALL = [(2, 4096, 16, 1, 512, 4), (1, 2048, 32, 1, 128, 2), (1, 3000, 16, 1, 256, 3),
+             (2, 384, 32, 2, 128, 1), (1, 200, 16, 1, 512, 2), (3, 8192, 16, 1, 128, 8)]
+
+
+@pytest.mark.parametrize("case", MQA_SMALL, ids=[str(c) for c in MQA_SMALL])
+def test_shared_kv_decode_matches_oracle(case):
+    b, L, hq, hkv, d, cp = case
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=L + 3 * d)
+    out, mo, lo = _decode(q, k, v, cp)
+    ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(out.cpu().numpy(), ref_out, f"mqa decode {case}")
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
+    lse = (mo + torch.log(lo)).cpu().numpy()
+    assert np.abs(lse - (ref_m + np.log(ref_l))).max() <= LSE_ABS
+
+
+def test_shared_kv_decode_with_k_equal_v():
+    # MLA-style: one latent per token serves as key and value (the same buffer twice)
+    b, L, hq, d, cp = 2, 4096, 16, 512, 4
+    q, k, _ = synth.decode_inputs(b, L, hq, 1, d, seed=77)
+    out, _, _ = _decode(q, k, k, cp)
+    ref_out, _, _ = OA.decode_attention(f64(q), f64(k), f64(k), 1.0 / math.sqrt(d))
+    assert_out_close(out.cpu().numpy(), ref_out, "mla-style")
+
+
+def test_shared_kv_decode_forced_rescales():
+    b, L, hq, d, cp = 1, 8192, 16, 256, 2
+    q, k, v = synth.decode_inputs(b, L, hq, 1, d, seed=78)
+    ramp = torch.linspace(0.0, 6.0, L, device="cuda").view(1, L, 1, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    q = (q.float() * 3.0).to(torch.bfloat16)
+    out, mo, lo = _decode(q, k, v, cp)
+    ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(out.cpu().numpy(), ref_out, "mqa rescale")
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS * 10
+
+
+def test_shared_kv_decode_workload_sampled():
+    """b8, 16 query heads on one 512-wide K/V head, L131072, cp8, at full size; sampled sequences."""
+    b, L, hq, d, cp = 8, 131072, 16, 512, 8
+    q, k, v = synth.decode_inputs(b, L, hq, 1, d, seed=20260006)
+    out, mo, lo = _decode(q, k, v, cp)
+    scale = 1.0 / math.sqrt(d)
+    for bi in (0, 5):
+        ref_out, ref_m, ref_l = OA.decode_attention(f64(q[bi:bi + 1]), f64(k[bi:bi + 1]), f64(v[bi:bi + 1]), scale)
+        assert_out_close(out[bi:bi + 1].cpu().numpy(), ref_out, f"mqa workload seq {bi}")
+        assert np.abs(mo[bi].cpu().numpy() - ref_m[0]).max() <= LSE_ABS
+    del q, k, v
+    torch.cuda.empty_cache()
+
+
 def test_decode_shards_do_not_change_the_answer():
     b, L, hq, hkv, d = 2, 4096, 4, 4, 128
     q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=3)

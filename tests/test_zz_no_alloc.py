@@ -69,7 +69,7 @@ def _close(got, ref):
 
 def test_noalloc_matches_workspace_decode_on_two_calls_in_a_row():
     # two different problems back to back: the second runs over the first one's leftovers
-    cases = [(8, 16384, 16, 16, 512, 8, 101), (3, 6144, 8, 2, 128, 3, 202)]
+    cases = [(8, 16384, 16, 16, 512, 8, 101), (3, 6144, 8, 2, 128, 3, 202), (4, 8192, 16, 1, 512, 4, 303)]
     results = []
     for b, L, hq, hkv, d, cp, seed in cases:
         q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=seed)
