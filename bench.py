@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "0daa7873e1af22f5", "bytes": 2252896752}
+RING_TRAFFIC = {"sha256_prefix": "4b46ed5b4b71f2cd", "bytes": 2246829616}
 
 
 def ring_traffic():
@@ -313,7 +313,7 @@ def bench_ours(args, rank, world, dist):
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": ring_traffic(),
                 "algorithmic_bytes": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + (o.numel() + 2 * m.numel()) * 4),
-                "kernel": "ring_attn_kernel<128>", "kernel_ms": round(kern_ms, 4),
+                "kernel": "ring_attn_kernel<128, balanced>", "kernel_ms": round(kern_ms, 4),
                 "peak_kind": f"bf16 sustained ({peaks['source']})",
                 "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
 

@@ -36,7 +36,7 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
 }
 
 template <int NCH>  // float4 slices of d owned by one lane (d <= 128 * NCH)
-__global__ void __launch_bounds__(kThreads) lse_merge_kernel(const __grid_constant__ MergeParams p) {
+__global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(const __grid_constant__ MergeParams p) {
   constexpr int kUnroll = (8 / NCH) < 2 ? 2 : (8 / NCH);  // parts in flight per lane
   extern __shared__ float smem[];
   const int n_parts = p.n_parts;
