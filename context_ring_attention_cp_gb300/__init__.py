@@ -24,7 +24,7 @@ __all__ = [
     "cp_plan_balanced_chunks", "cp_plan_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn",
     "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
-    "cp_merge_tree_workspace_bytes", "cp_merge_partials_tree",
+    "cp_merge_tree_workspace_bytes", "cp_merge_partials_tree", "cp_selftest_wait_timeout",
 ]
 
 CP_OK = 0
@@ -103,6 +103,7 @@ def load_library():
         "cp_merge_partials_tree": (_I32, [_I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P,
                                           _I32, _P]),
         "cp_passq_decode_noalloc": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P]),
+        "cp_selftest_wait_timeout": (_I32, [_P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -265,6 +266,11 @@ def cp_passq_decode_noalloc(desc: AttnDesc, q, k, v, out, m_out=None, l_out=None
         raise CpError(st, "cp_passq_decode_noalloc (unsupported shape, or partials larger than the "
                           f"{CP_PASSQ_NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)")
     _check(st, "cp_passq_decode_noalloc")
+
+
+def cp_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (records CP_ERR_TIMEOUT after about a second)."""
+    _check(load_library().cp_selftest_wait_timeout(_stream(stream)), "cp_selftest_wait_timeout")
 
 
 def cp_take_device_status(stream=None) -> int:

@@ -371,6 +371,10 @@ cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const
   return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
+cp_status cp_selftest_wait_timeout(void* cuda_stream) {
+  return ring_wait_timeout_selftest(static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+}
+
 cp_status cp_take_device_status(void* cuda_stream, int32_t* status) {
   if (status == nullptr) return CP_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CP_ERR_CUDA;

@@ -58,5 +58,7 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
                            cudaStream_t stream);
 // Reads and clears the ring kernel's device status word (after the caller synchronised).
 cudaError_t ring_take_status(int32_t* status);
+// Launches one CTA whose bounded wait can never complete (records CP_ERR_TIMEOUT).
+cudaError_t ring_wait_timeout_selftest(cudaStream_t stream);
 
 }  // namespace cpattn

@@ -568,6 +568,23 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 // Host side
 // ---------------------------------------------------------------------------
 
+// One CTA waits, with the ring kernel's bounded wait, on an mbarrier that nothing
+// will ever complete: after about a second the wait gives up and records
+// CP_ERR_TIMEOUT in the ring kernel's status word, exactly as a stalled ring
+// launch would.  Used to test the failure path without faulting the GPU.
+__global__ void ring_wait_timeout_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, &abort_flag);
+  __syncthreads();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
@@ -647,6 +664,11 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
                       : launch_d<64, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream);
   return d.d == 128 ? launch_d<128, CP_LAYOUT_BALANCED>(p, n_items, stream)
                     : launch_d<64, CP_LAYOUT_BALANCED>(p, n_items, stream);
+}
+
+cudaError_t ring_wait_timeout_selftest(cudaStream_t stream) {
+  ring_wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
 }
 
 cudaError_t ring_take_status(int32_t* status) {

@@ -291,6 +291,18 @@ CPATTN_API cp_status cp_comm_bytes(const cp_comm_query* query, cp_comm_result* r
  */
 CPATTN_API cp_status cp_take_device_status(void* cuda_stream, int32_t* status);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages, which leave failure
+ * handling out; their design rationale forbids silent fallbacks).  Launches one
+ * CTA on `cuda_stream` that waits, with the same bounded mbarrier wait the ring
+ * kernel uses, on a barrier nothing will complete.  After about one second the
+ * wait gives up and records CP_ERR_TIMEOUT in the ring kernel's device status
+ * word; until cp_take_device_status() clears it, ring launches return at once
+ * without writing.  Nothing faults, traps or hangs.
+ * Errors: a failed launch -> CP_ERR_CUDA.
+ */
+CPATTN_API cp_status cp_selftest_wait_timeout(void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -230,6 +230,30 @@ def test_rank_ranges_touch_only_their_rows_and_compose(layout):
         assert torch.equal(x, y)
 
 
+def test_bounded_wait_timeout_is_reported_and_recovers():
+    """A wait that nothing completes gives up (about 1 s), records CP_ERR_TIMEOUT,
+    ring launches skip their work until the status is taken, then work again."""
+    import time
+    assert cpa.cp_take_device_status() == 0
+    b, S, hq, hkv, d, cp = 1, 512, 2, 2, 64, 2
+    q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=41)
+    t0 = time.time()
+    cpa.cp_selftest_wait_timeout()
+    bufs = ring_buffers(b, S, hq, d)
+    for x in bufs:
+        x.fill_(float("nan"))
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+    cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, *bufs, EMIT | FIN)  # queued behind the stalled wait
+    torch.cuda.synchronize()
+    assert 0.5 < time.time() - t0 < 30.0
+    assert all(torch.isnan(x).all() for x in bufs), "a ring launch ran while the status word held an error"
+    assert cpa.cp_take_device_status() == cpa.CP_ERR_TIMEOUT
+    assert cpa.cp_take_device_status() == 0  # taken: cleared
+    o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    ref_out, _, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(o.cpu().numpy(), ref_out, "after recovery")
+
+
 @pytest.mark.parametrize("name", ["gqa", "long"])
 def test_full_size_workload_sampled_rows(name):
     """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled."""
