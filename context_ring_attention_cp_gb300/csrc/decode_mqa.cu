@@ -8,7 +8,8 @@
 // shapes), every K/V byte feeds 16 dot products: at HBM speed that is ~16 FLOP/B,
 // beyond the FP32 pipes, so both contractions run on tcgen05.
 //
-// Transposed formulation, one CTA per (KV range, sequence, kv head):
+// Transposed formulation; one persistent CTA per SM walks work items (KV range,
+// sequence, kv head) strided by the grid, keeping its barriers, ring and TMEM:
 //   S^T = K Q^T   M = 128 keys, N = g heads, K = d      (A = K tile, B = Q, both K-major)
 //   O^T += V^T P^T  M = 128-wide d block, N = g, K = 128 keys
 //                   (A = V tile read MN-major, B = P^T written by the softmax warps)
@@ -26,6 +27,10 @@
 // grows by more than 8 (log2 units), O^T columns are then rescaled in TMEM.  Row
 // sums stay per thread until the epilogue.  The CTA writes its partial triple per
 // query head to the decode workspace, which the LSE merge kernel reduces.
+//
+// Across items: Q is double-buffered (released after an item's last S^T), and the
+// next item's first O^T waits until the epilogue has read the previous O^T out of
+// TMEM, so the next item's first S^T overlaps the previous epilogue.
 //
 // Every mbarrier wait is bounded (tc_ptx.h); on expiry CP_ERR_TIMEOUT goes to this
 // file's status word and the CTA returns.
@@ -62,9 +67,9 @@ struct MqaCfg {
   static constexpr int kQBytes = kSlabsPerTile * kQSlab;
   static constexpr int kPSlab = G * 128;            // bytes of one P^T slab (G rows x 64 keys)
   static constexpr int kPBytes = 2 * kPSlab;        // one P^T buffer (128 keys)
-  static constexpr int kSlots = (G == 16) ? 12 : 10;  // even ring size
-  static constexpr int kQOff = 0;
-  static constexpr int kPOff = kQBytes;             // two P^T buffers
+  static constexpr int kSlots = (G == 16) ? 10 : 8;  // even ring size
+  static constexpr int kQOff = 0;                   // two Q buffers (consecutive work items)
+  static constexpr int kPOff = 2 * kQBytes;         // two P^T buffers
   static constexpr int kRingOff = kPOff + 2 * kPBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kSlabBytes;
   static constexpr int kRedOff = kBarOff + 512;     // [2][4][G] per-warp maxima, then [4][G] row sums
@@ -86,7 +91,8 @@ struct MqaParams {
   int64_t b, L, h_q, h_kv;
   int64_t part_len;
   int32_t n_parts;
-  float sl;  // scale * log2(e)
+  int32_t n_items;  // n_parts * b * h_kv work items, strided over the persistent grid
+  float sl;         // scale * log2(e)
 };
 
 template <int D, int G>
@@ -97,38 +103,39 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::kBarOff);
-  const uint32_t bar_q = smem_u32(&bars[0]);
-  auto bar_full = [&](int s) { return smem_u32(&bars[1 + s]); };
-  auto bar_empty = [&](int s) { return smem_u32(&bars[1 + K::kSlots + s]); };
-  auto bar_s = [&](int b) { return smem_u32(&bars[1 + 2 * K::kSlots + b]); };
-  auto bar_p = [&](int b) { return smem_u32(&bars[3 + 2 * K::kSlots + b]); };
-  const uint32_t bar_o = smem_u32(&bars[5 + 2 * K::kSlots]);
-  const uint32_t bar_red = smem_u32(&bars[6 + 2 * K::kSlots]);  // the four softmax warps, one phase per tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[7 + 2 * K::kSlots]);
+  auto bar_qf = [&](int b) { return smem_u32(&bars[0 + b]); };   // Q buffer b loaded
+  auto bar_qe = [&](int b) { return smem_u32(&bars[2 + b]); };   // Q buffer b no longer read
+  auto bar_full = [&](int s) { return smem_u32(&bars[4 + s]); };
+  auto bar_empty = [&](int s) { return smem_u32(&bars[4 + K::kSlots + s]); };
+  auto bar_s = [&](int b) { return smem_u32(&bars[4 + 2 * K::kSlots + b]); };
+  auto bar_p = [&](int b) { return smem_u32(&bars[6 + 2 * K::kSlots + b]); };
+  const uint32_t bar_o = smem_u32(&bars[8 + 2 * K::kSlots]);      // O^T of a tile complete
+  const uint32_t bar_of = smem_u32(&bars[9 + 2 * K::kSlots]);     // O^T read by the epilogue
+  const uint32_t bar_red = smem_u32(&bars[10 + 2 * K::kSlots]);   // the four softmax warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[11 + 2 * K::kSlots]);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(smem + K::kRedOff);  // [2][4][G] maxima
   float* red_l = red + 2 * 4 * G;                             // [4][G] row sums
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int part = blockIdx.x;
-  const int64_t bk = blockIdx.y;  // sequence * h_kv + kv head
-  const int32_t kvh = int32_t(bk % p.h_kv);
-  const int32_t bi = int32_t(bk / p.h_kv);
-  const int64_t k_begin = int64_t(part) * p.part_len;
-  const int64_t k_end = k_begin + p.part_len;
-  const int32_t n_tiles = int32_t((p.part_len + BK - 1) / BK);
+  const int32_t n_tiles = int32_t((p.part_len + BK - 1) / BK);  // the same for every item
+  // work item -> (key range, sequence, kv head)
+  auto item_part = [&](int32_t item) { return item % p.n_parts; };
+  auto item_bk = [&](int32_t item) { return int64_t(item / p.n_parts); };
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_qf(b), 1);
+      mbar_init(bar_qe(b), 1);
+      mbar_init(bar_s(b), 1);
+      mbar_init(bar_p(b), 4);
+    }
     for (int s = 0; s < K::kSlots; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s(b), 1);
-      mbar_init(bar_p(b), 4);
-    }
     mbar_init(bar_o, 1);
+    mbar_init(bar_of, 4);
     mbar_init(bar_red, 4);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_mqa_status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -150,24 +157,34 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(bar_q, uint32_t(K::kQBytes));
-      for (int sl = 0; sl < NS; ++sl)
-        tma_load_3d(sbase + K::kQOff + sl * K::kQSlab, &p.tmap_q, bar_q, sl * 64, kvh * G, bi);
-      int32_t li = 0;  // running load index, in MMA consumption order
+      int32_t li = 0;  // running slab index, in MMA consumption order
       bool ok = true;
-      auto load_tile = [&](const CUtensorMap* map, int32_t tile) {
-        const int32_t key0 = int32_t(k_begin) + tile * BK;
-        for (int sl = 0; sl < NS && ok; ++sl, ++li) {
-          const int s = li % K::kSlots, round = li / K::kSlots;
-          if (round > 0 && !wait(bar_empty(s), uint32_t((round - 1) & 1))) { ok = false; break; }
-          mbar_expect_tx(bar_full(s), uint32_t(kSlabBytes));
-          tma_load_4d(sbase + K::kRingOff + s * kSlabBytes, map, bar_full(s), sl * 64, kvh, key0, bi);
+      int32_t ic = 0;  // items of this CTA so far
+      for (int32_t item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++ic) {
+        const int32_t part = item_part(item);
+        const int64_t bk = item_bk(item);
+        const int32_t kvh = int32_t(bk % p.h_kv), bi = int32_t(bk / p.h_kv);
+        const int32_t k_begin = int32_t(int64_t(part) * p.part_len);
+        const int qb = ic & 1;
+        if (ic >= 2 && !wait(bar_qe(qb), uint32_t(((ic >> 1) - 1) & 1))) { ok = false; break; }
+        mbar_expect_tx(bar_qf(qb), uint32_t(K::kQBytes));
+        for (int sl = 0; sl < NS; ++sl)
+          tma_load_3d(sbase + K::kQOff + qb * K::kQBytes + sl * K::kQSlab, &p.tmap_q, bar_qf(qb), sl * 64, kvh * G,
+                      bi);
+        auto load_tile = [&](const CUtensorMap* map, int32_t tile) {
+          const int32_t key0 = k_begin + tile * BK;
+          for (int sl = 0; sl < NS && ok; ++sl, ++li) {
+            const int s = li % K::kSlots, round = li / K::kSlots;
+            if (round > 0 && !wait(bar_empty(s), uint32_t((round - 1) & 1))) { ok = false; break; }
+            mbar_expect_tx(bar_full(s), uint32_t(kSlabBytes));
+            tma_load_4d(sbase + K::kRingOff + s * kSlabBytes, map, bar_full(s), sl * 64, kvh, key0, bi);
+          }
+        };
+        load_tile(&p.tmap_k, 0);
+        for (int32_t j = 0; ok && j < n_tiles; ++j) {
+          if (j + 1 < n_tiles) load_tile(&p.tmap_k, j + 1);
+          if (ok) load_tile(&p.tmap_v, j);
         }
-      };
-      load_tile(&p.tmap_k, 0);
-      for (int32_t j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) load_tile(&p.tmap_k, j + 1);
-        if (ok) load_tile(&p.tmap_v, j);
       }
       if (!ok) {
         const uint64_t t0 = globaltimer();
@@ -180,61 +197,72 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
     if (lane == 0) {
       constexpr uint32_t idesc_s = instr_desc_bf16(128, G, false, false);
       constexpr uint32_t idesc_o = instr_desc_bf16(128, G, true, false);
-      int32_t li = 0;
-      bool ok = wait(bar_q, 0);
-      // S^T(j) into S buffer j % 2 from the K slabs of tile j (next NS slots in order)
-      auto issue_s = [&](int32_t j) {
-        const uint32_t d_tm = tmem + uint32_t(j & 1) * G;
-        for (int sl = 0; sl < NS && ok; ++sl, ++li) {
-          const int s = li % K::kSlots;
-          if (!wait(bar_full(s), uint32_t((li / K::kSlots) & 1))) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ka = sbase + K::kRingOff + s * kSlabBytes;
-          const uint32_t qa = sbase + K::kQOff + sl * K::kQSlab;
+      int32_t li = 0;   // running slab index
+      int32_t jt = 0;   // running tile index (S / P buffer and barrier phases)
+      bool ok = true;
+      int32_t ic = 0;
+      for (int32_t item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++ic) {
+        const int qb = ic & 1;
+        if (!wait(bar_qf(qb), uint32_t((ic >> 1) & 1))) { ok = false; break; }
+        // S^T of global tile t into S buffer t % 2 from the next NS K slabs
+        auto issue_s = [&](int32_t t) {
+          const uint32_t d_tm = tmem + uint32_t(t & 1) * G;
+          for (int sl = 0; sl < NS && ok; ++sl, ++li) {
+            const int s = li % K::kSlots;
+            if (!wait(bar_full(s), uint32_t((li / K::kSlots) & 1))) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ka = sbase + K::kRingOff + s * kSlabBytes;
+            const uint32_t qa = sbase + K::kQOff + qb * K::kQBytes + sl * K::kQSlab;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // 16 d per k-step = 32 bytes into the 128-byte row
-            mma_ss(d_tm, smem_desc(ka + kk * 32, 16, 1024), smem_desc(qa + kk * 32, 16, 1024), idesc_s,
-                   (sl > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar_empty(s));
-        }
-      };
-      // O^T += V^T(j) P^T(j): d blocks of 128 = slab pairs, 8 k-steps of 16 keys each
-      auto issue_o = [&](int32_t j) {
-        const uint32_t pa = sbase + K::kPOff + uint32_t(j & 1) * K::kPBytes;
-        for (int blk = 0; blk < NS / 2 && ok; ++blk, li += 2) {
-          const int s0 = li % K::kSlots, s1 = (li + 1) % K::kSlots;
-          if (!wait(bar_full(s0), uint32_t((li / K::kSlots) & 1)) ||
-              !wait(bar_full(s1), uint32_t(((li + 1) / K::kSlots) & 1))) {
-            ok = false;
-            break;
+            for (int kk = 0; kk < 4; ++kk)  // 16 d per k-step = 32 bytes into the 128-byte row
+              mma_ss(d_tm, smem_desc(ka + kk * 32, 16, 1024), smem_desc(qa + kk * 32, 16, 1024), idesc_s,
+                     (sl > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar_empty(s));
           }
-          tc_fence_after();
-          const uint32_t va = sbase + K::kRingOff + s0 * kSlabBytes;  // s1 == s0 + 1 (even slot, even ring)
-          const uint32_t d_tm = tmem + K::kOCol + uint32_t(blk) * G;
+        };
+        // O^T += V^T(t) P^T(t): d blocks of 128 = slab pairs, 8 k-steps of 16 keys each
+        auto issue_o = [&](int32_t t, bool first) {
+          const uint32_t pa = sbase + K::kPOff + uint32_t(t & 1) * K::kPBytes;
+          for (int blk = 0; blk < NS / 2 && ok; ++blk, li += 2) {
+            const int s0 = li % K::kSlots, s1 = (li + 1) % K::kSlots;
+            if (!wait(bar_full(s0), uint32_t((li / K::kSlots) & 1)) ||
+                !wait(bar_full(s1), uint32_t(((li + 1) / K::kSlots) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t va = sbase + K::kRingOff + s0 * kSlabBytes;  // s1 == s0 + 1 (even slot, even ring)
+            const uint32_t d_tm = tmem + K::kOCol + uint32_t(blk) * G;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_ss(d_tm, smem_desc(va + kk * 2048, kSlabBytes, 1024),
-                   smem_desc(pa + (kk / 4) * K::kPSlab + (kk % 4) * 32, 16, 1024), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar_empty(s0));
-          mma_commit(bar_empty(s1));
-        }
-      };
-      if (ok) {
-        issue_s(0);
-        if (ok) mma_commit(bar_s(0));
-      }
-      for (int32_t j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) {
-          issue_s(j + 1);
-          if (!ok) break;
-          mma_commit(bar_s((j + 1) & 1));
-        }
-        if (!wait(bar_p(j & 1), uint32_t((j >> 1) & 1))) { ok = false; break; }
-        tc_fence_after();
-        issue_o(j);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_ss(d_tm, smem_desc(va + kk * 2048, kSlabBytes, 1024),
+                     smem_desc(pa + (kk / 4) * K::kPSlab + (kk % 4) * 32, 16, 1024), idesc_o,
+                     (!first || kk > 0) ? 1u : 0u);
+            mma_commit(bar_empty(s0));
+            mma_commit(bar_empty(s1));
+          }
+        };
+        issue_s(jt);
         if (!ok) break;
-        mma_commit(bar_o);
+        mma_commit(bar_s(jt & 1));
+        if (n_tiles == 1) mma_commit(bar_qe(qb));
+        for (int32_t j = 0; ok && j < n_tiles; ++j) {
+          const int32_t t = jt + j;
+          if (j + 1 < n_tiles) {
+            issue_s(t + 1);
+            if (!ok) break;
+            mma_commit(bar_s((t + 1) & 1));
+            if (j + 2 == n_tiles) mma_commit(bar_qe(qb));  // the item's last S^T: Q buffer free
+          }
+          if (!wait(bar_p(t & 1), uint32_t((t >> 1) & 1))) { ok = false; break; }
+          // the previous item's O^T must have been read out before this item overwrites it
+          if (j == 0 && ic > 0 && !wait(bar_of, uint32_t((ic - 1) & 1))) { ok = false; break; }
+          tc_fence_after();
+          issue_o(t, j == 0);
+          if (!ok) break;
+          mma_commit(bar_o);
+        }
+        jt += n_tiles;
       }
       if (!ok) {
         const uint64_t t0 = globaltimer();
@@ -244,112 +272,124 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int t = threadIdx.x - 128;  // key lane of S^T, d lane of O^T
+    const int t_ = threadIdx.x - 128;  // key lane of S^T, d lane of O^T
     const int wq = warp - 4;
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
-    float m_ref[G], m_true[G], l_t[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m_ref[h] = -INFINITY;
-      m_true[h] = -INFINITY;
-      l_t[h] = 0.f;
-    }
     bool ok = true;
-    for (int32_t j = 0; j < n_tiles; ++j) {
-      if (!__all_sync(0xffffffffu, wait(bar_s(j & 1), uint32_t((j >> 1) & 1)))) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[G];
-      if constexpr (G == 16) {
-        tmem_ld16(tmem + lane_base + uint32_t(j & 1) * G, sr);
-        tmem_ld_wait16(sr);
-      } else {
-        tmem_ld32(tmem + lane_base + uint32_t(j & 1) * G, sr);
-        tmem_ld_wait(sr);
-      }
-      const int64_t key = k_begin + int64_t(j) * BK + t;
-      const bool valid = key < k_end;
-      float x[G], mx[G];
+    int32_t jt = 0;  // running tile index
+    int32_t rc = 0;  // running phase of the cross-warp barrier
+    for (int32_t item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      const int32_t part = item_part(item);
+      const int64_t bk = item_bk(item);
+      const int32_t kvh = int32_t(bk % p.h_kv), bi = int32_t(bk / p.h_kv);
+      const int64_t k_begin = int64_t(part) * p.part_len;
+      const int64_t k_end = k_begin + p.part_len;
+      float m_ref[G], m_true[G], l_t[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        x[h] = valid ? __uint_as_float(sr[h]) : -INFINITY;
-        mx[h] = x[h];
+        m_ref[h] = -INFINITY;
+        m_true[h] = -INFINITY;
+        l_t[h] = 0.f;
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
-      }
-      // Cross-warp maxima through shared memory, double-buffered by tile parity; the
-      // barrier is an mbarrier (bounded wait), not bar.sync, so a warp that gave up
-      // cannot leave the others waiting forever.
-      float* rb = red + (j & 1) * 4 * G;
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) rb[wq * G + h] = mx[h];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_red);
-      if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(j & 1)))) { ok = false; break; }
-      bool any_raise = false;
-      float f[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float tmax = fmaxf(fmaxf(rb[h], rb[G + h]), fmaxf(rb[2 * G + h], rb[3 * G + h])) * p.sl;
-        m_true[h] = fmaxf(m_true[h], tmax);
-        const bool raise = tmax > m_ref[h] + kRescaleThreshold;
-        f[h] = 1.f;
-        if (raise) {
-          f[h] = (m_ref[h] == -INFINITY) ? 0.f : ex2(m_ref[h] - tmax);
-          any_raise = any_raise || (j > 0 && m_ref[h] != -INFINITY);
-          l_t[h] *= f[h];
-          m_ref[h] = tmax;
+      for (int32_t j = 0; j < n_tiles; ++j) {
+        const int32_t t = jt + j;
+        if (!__all_sync(0xffffffffu, wait(bar_s(t & 1), uint32_t((t >> 1) & 1)))) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[G];
+        if constexpr (G == 16) {
+          tmem_ld16(tmem + lane_base + uint32_t(t & 1) * G, sr);
+          tmem_ld_wait16(sr);
+        } else {
+          tmem_ld32(tmem + lane_base + uint32_t(t & 1) * G, sr);
+          tmem_ld_wait(sr);
         }
-      }
-      // O^T(j-1) complete before it is rescaled and before P buffer j%2 (read by O^T(j-2)) is rewritten
-      if (j > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((j - 1) & 1)))) { ok = false; break; }
-      tc_fence_after();
-      if (any_raise) {  // identical in every thread: decided from the shared maxima
+        const int64_t key = k_begin + int64_t(j) * BK + t_;
+        const bool valid = key < k_end;
+        float x[G], mx[G];
 #pragma unroll
-        for (int blk = 0; blk < D / 128; ++blk) {
-          const uint32_t oaddr = tmem + lane_base + K::kOCol + uint32_t(blk) * G;
-          uint32_t r[G];
-          if constexpr (G == 16) {
-            tmem_ld16(oaddr, r);
-            tmem_ld_wait16(r);
+        for (int h = 0; h < G; ++h) {
+          x[h] = valid ? __uint_as_float(sr[h]) : -INFINITY;
+          mx[h] = x[h];
+        }
 #pragma unroll
-            for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
-            tmem_st16(oaddr, r);
-          } else {
-            tmem_ld32(oaddr, r);
-            tmem_ld_wait(r);
+        for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
-            for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
-            tmem_st32(oaddr, r);
+          for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+        }
+        // Cross-warp maxima through shared memory, double-buffered by phase; the
+        // barrier is an mbarrier (bounded wait), not bar.sync, so a warp that gave
+        // up cannot leave the others waiting forever.
+        float* rb = red + (rc & 1) * 4 * G;
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) rb[wq * G + h] = mx[h];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_red);
+        if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(rc & 1)))) { ok = false; break; }
+        ++rc;
+        bool any_raise = false;
+        float f[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float tmax = fmaxf(fmaxf(rb[h], rb[G + h]), fmaxf(rb[2 * G + h], rb[3 * G + h])) * p.sl;
+          m_true[h] = fmaxf(m_true[h], tmax);
+          const bool raise = tmax > m_ref[h] + kRescaleThreshold;
+          f[h] = 1.f;
+          if (raise) {
+            f[h] = (m_ref[h] == -INFINITY) ? 0.f : ex2(m_ref[h] - tmax);
+            any_raise = any_raise || (j > 0 && m_ref[h] != -INFINITY);
+            l_t[h] *= f[h];
+            m_ref[h] = tmax;
           }
         }
-        tmem_st_wait();
-      }
-      // P^T(j): row h, key column t of a [G x 128] K-major, 128-byte-swizzled operand
-      uint8_t* pbuf = smem + K::kPOff + (j & 1) * K::kPBytes + (t / 64) * K::kPSlab;
-      const int c16 = (t % 64) / 8, within = (t % 8) * 2;
+        // O^T of the previous tile complete before it is rescaled and before P buffer
+        // t % 2 (read by tile t - 2) is rewritten; at an item's first tile the previous
+        // item's epilogue already waited for it.
+        if (j > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((t - 1) & 1)))) { ok = false; break; }
+        tc_fence_after();
+        if (any_raise) {  // identical in every thread: decided from the shared maxima
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pv = ex2(fmaf(x[h], p.sl, -((m_ref[h] == -INFINITY) ? 0.f : m_ref[h])));
-        l_t[h] += pv;
-        const __nv_bfloat16 bv = __float2bfloat16_rn(pv);
-        *reinterpret_cast<__nv_bfloat16*>(pbuf + h * 128 + ((c16 ^ (h % 8)) << 4) + within) = bv;
+          for (int blk = 0; blk < D / 128; ++blk) {
+            const uint32_t oaddr = tmem + lane_base + K::kOCol + uint32_t(blk) * G;
+            uint32_t r[G];
+            if constexpr (G == 16) {
+              tmem_ld16(oaddr, r);
+              tmem_ld_wait16(r);
+#pragma unroll
+              for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
+              tmem_st16(oaddr, r);
+            } else {
+              tmem_ld32(oaddr, r);
+              tmem_ld_wait(r);
+#pragma unroll
+              for (int h = 0; h < G; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * f[h]);
+              tmem_st32(oaddr, r);
+            }
+          }
+          tmem_st_wait();
+        }
+        // P^T(t): row h, key column t_ of a [G x 128] K-major, 128-byte-swizzled operand
+        uint8_t* pbuf = smem + K::kPOff + (t & 1) * K::kPBytes + (t_ / 64) * K::kPSlab;
+        const int c16 = (t_ % 64) / 8, within = (t_ % 8) * 2;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pv = ex2(fmaf(x[h], p.sl, -((m_ref[h] == -INFINITY) ? 0.f : m_ref[h])));
+          l_t[h] += pv;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + h * 128 + ((c16 ^ (h % 8)) << 4) + within) =
+              __float2bfloat16_rn(pv);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p(t & 1));
       }
-      fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(j & 1));
-    }
+      if (!ok) break;
 
-    // ---------------- epilogue: this range's partial triple per query head
-    if (ok && n_tiles > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((n_tiles - 1) & 1)))) ok = false;
-    if (ok) {
+      // ---------------- epilogue: this item's partial triple per query head
+      const int32_t t_last = jt + n_tiles - 1;
+      if (!__all_sync(0xffffffffu, wait(bar_o, uint32_t(t_last & 1)))) { ok = false; break; }
       tc_fence_after();
-      // row sums over the 128 key lanes: butterfly, then the four warps
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
@@ -361,9 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_red);
-      if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(n_tiles & 1)))) ok = false;
-    }
-    if (ok) {
+      if (!__all_sync(0xffffffffu, wait(bar_red, uint32_t(rc & 1)))) { ok = false; break; }
+      ++rc;
       const int64_t row0 = (int64_t(part) * p.b + bi) * p.h_q + int64_t(kvh) * G;
 #pragma unroll
       for (int blk = 0; blk < D / 128; ++blk) {
@@ -380,23 +419,28 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
         for (int h = 0; h < G; ++h) {
           // re-express against the true max: factor 2^(m_ref - m_true) <= 1
           const float fre = (m_true[h] == -INFINITY) ? 0.f : ex2(m_ref[h] - m_true[h]);
-          p.o_parts[(row0 + h) * D + blk * 128 + t] = __uint_as_float(r[h]) * fre;
+          p.o_parts[(row0 + h) * D + blk * 128 + t_] = __uint_as_float(r[h]) * fre;
         }
       }
-      if (t < G) {
-        float lsum = 0.f, mt = 0.f, mr = 0.f;
+      // O^T has been read into registers: the next item may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_of);
+      if (t_ < G) {
+        float mt = 0.f, mr = 0.f;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          if (h == t) {
+          if (h == t_) {
             mt = m_true[h];
             mr = m_ref[h];
           }
         }
-        lsum = red_l[t] + red_l[G + t] + red_l[2 * G + t] + red_l[3 * G + t];
+        const float lsum = red_l[t_] + red_l[G + t_] + red_l[2 * G + t_] + red_l[3 * G + t_];
         const float fre = (mt == -INFINITY) ? 0.f : ex2(mr - mt);
-        p.m_parts[row0 + t] = mt * kLn2;  // natural-log units
-        p.l_parts[row0 + t] = lsum * fre;
+        p.m_parts[row0 + t_] = mt * kLn2;  // natural-log units
+        p.l_parts[row0 + t_] = lsum * fre;
       }
+      jt += n_tiles;
     }
   }
 
@@ -450,7 +494,7 @@ bool decode_mqa_supported(const cp_attn_desc& d) {
          d.b <= 65535 && d.h_kv <= 65535;
 }
 
-// Ranges of at least 512 keys, about four waves of one CTA per SM.
+// Ranges of at least 512 keys, about four work items per SM.
 int32_t decode_mqa_splits(const cp_attn_desc& d, int sm_count) {
   const int64_t shard = d.S / d.cp;
   const int64_t groups = d.b * d.h_kv * d.cp;
@@ -491,7 +535,14 @@ cudaError_t launch_decode_mqa(const cp_attn_desc& d, int32_t splits, const void*
   p.n_parts = int32_t(d.cp * splits);
   p.part_len = d.S / p.n_parts;
   p.sl = d.scale * kLog2e;
-  const dim3 grid(unsigned(p.n_parts), unsigned(d.b * d.h_kv));
+  const int64_t n_items = int64_t(p.n_parts) * d.b * d.h_kv;
+  if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  p.n_items = int32_t(n_items);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(unsigned(n_items < sms ? n_items : sms));  // persistent: one CTA per SM
 #define CP_MQA(DD, GG) \
   if (d.d == DD && G == GG) return launch_dg<DD, GG>(p, grid, stream);
   CP_MQA(128, 16) CP_MQA(256, 16) CP_MQA(512, 16)
