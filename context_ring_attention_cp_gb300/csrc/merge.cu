@@ -143,9 +143,102 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(c
   }
 }
 
+// rows == 1 (the decode reduce: one triple per sequence and head): one CTA per
+// (batch, head).  The part weights e^{m_p - m} are computed once into shared
+// memory, then each thread streams a float4 slice of d through every part in the
+// caller's order.
+__global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_constant__ MergeParams p) {
+  extern __shared__ float smem[];
+  float* w = smem;                             // [n_parts] weights in fold order
+  float* red = smem + CP_MAX_MERGE_PARTS;      // [kWarps] partial maxima / sums
+  const int n = p.n_parts;
+  const int64_t bh = blockIdx.x;
+  const int64_t h = bh % p.heads, bi = bh / p.heads;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  auto ml_off = [&](int part) { return (int64_t(part) * p.batch + bi) * p.heads + h; };  // rows == 1
+
+  float mx = -INFINITY;
+  for (int k = threadIdx.x; k < n; k += kThreads) {
+    const float m = p.m_parts[ml_off(p.order[k])];
+    w[k] = m;
+    mx = fmaxf(mx, m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int i = 1; i < kWarps; ++i) mx = fmaxf(mx, red[i]);
+  const float shift = (mx == -INFINITY) ? 0.f : mx;  // all parts the identity: stays the identity
+  __syncthreads();
+  float ls = 0.f;
+  for (int k = threadIdx.x; k < n; k += kThreads) {
+    const float wk = expf(w[k] - shift);
+    w[k] = wk;
+    ls = fmaf(wk, p.l_parts[ml_off(p.order[k])], ls);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+  if (lane == 0) red[warp] = ls;
+  __syncthreads();
+  float lsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) lsum += red[i];
+
+  const int64_t n_vec = p.d / 4;
+  const int64_t part_stride = p.batch * p.heads * p.d;  // rows == 1
+  const int64_t obase = (bi * p.heads + h) * p.d;
+  const float inv = (p.finalize && lsum > 0.f) ? 1.f / lsum : 1.f;
+  const bool zero = p.finalize && !(lsum > 0.f);
+  for (int64_t c = threadIdx.x; c < n_vec; c += kThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int k = 0;
+    for (; k + 4 <= n; k += 4) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        x[u] = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(p.order[k + u]) * part_stride + obase) + c);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wk = w[k + u];
+        acc.x = fmaf(wk, x[u].x, acc.x);
+        acc.y = fmaf(wk, x[u].y, acc.y);
+        acc.z = fmaf(wk, x[u].z, acc.z);
+        acc.w = fmaf(wk, x[u].w, acc.w);
+      }
+    }
+    for (; k < n; ++k) {
+      const float4 x = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(p.order[k]) * part_stride + obase) + c);
+      const float wk = w[k];
+      acc.x = fmaf(wk, x.x, acc.x);
+      acc.y = fmaf(wk, x.y, acc.y);
+      acc.z = fmaf(wk, x.z, acc.z);
+      acc.w = fmaf(wk, x.w, acc.w);
+    }
+    if (zero) {
+      acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (p.finalize) {
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    }
+    reinterpret_cast<float4*>(p.o_out + obase)[c] = acc;
+  }
+  if (threadIdx.x == 0) {
+    if (p.m_out) p.m_out[bi * p.heads + h] = mx;
+    if (p.l_out) p.l_out[bi * p.heads + h] = lsum;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  if (p.rows == 1) {
+    const int64_t ctas = p.batch * p.heads;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const size_t smem = (CP_MAX_MERGE_PARTS + kWarps) * sizeof(float);
+    lse_merge_rows1_kernel<<<unsigned(ctas), kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t tiles = row_blocks * p.batch * p.heads;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
