@@ -309,13 +309,16 @@ def bench_ours(args, rank, world, dist):
 
     kern_ms = statistics.mean(kernel_ms)
     achieved = flops / (kern_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # The step is this one kernel, timed alone in a sub-second loop (the clocks record
+    # shows whether the power cap engaged): the burst GEMM peak is the denominator,
+    # the sustained one is reported beside it.
+    peak = peaks["bf16_tflops"]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": ring_traffic(),
                 "algorithmic_bytes": int(q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + (o.numel() + 2 * m.numel()) * 4),
                 "kernel": "ring_attn_kernel<128, balanced>", "kernel_ms": round(kern_ms, 4),
-                "peak_kind": f"bf16 sustained ({peaks['source']})",
-                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)}
+                "peak_kind": f"bf16 burst ({peaks['source']})",
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
 
     # ---- end to end through the C-ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -401,7 +404,7 @@ def secondary_lines(cpa, synth, peaks, stream):
     out["prefill_one_step_emit"] = {
         "workload": "one ring step (t=1, all 8 virtual ranks, EMIT) of the GQA prefill workload",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
-        "peak": peaks["bf16_tflops_sustained"], "frac": round(tf / peaks["bf16_tflops_sustained"], 4)}
+        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # per-virtual-rank work under the balanced (method) and sequential (plain) layouts:
@@ -442,8 +445,7 @@ def secondary_lines(cpa, synth, peaks, stream):
     tf = prefill_flops(w) / (ms * 1e-3) / 1e12
     out["prefill_long"] = {"workload": "prefill ring attention, long: b1, 32/8 heads, d128, S131072, cp16",
                            "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 3), "flops": prefill_flops(w),
-                           "peak": peaks["bf16_tflops_sustained"],
-                           "frac": round(tf / peaks["bf16_tflops_sustained"], 4)}
+                           "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)

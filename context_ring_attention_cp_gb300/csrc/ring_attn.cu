@@ -30,7 +30,7 @@
 //
 // Per CTA (384 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a ring of smem slots
-//   warp 1      TMEM owner and MMA issuer (one lane): S = Q K^T and O += P V
+//   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane issues)
 //   warps 4-7   softmax of query tile A (thread = row = TMEM lane)
 //   warps 8-11  softmax of query tile B
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B.  P (bf16)
@@ -280,12 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
   // Register split (launched with 168 per thread, 64,512 in all): the producer /
   // MMA warpgroup gives registers to the two softmax warpgroups.
-  // 128 x 56 + 256 x 216 = 62,464 <= 64,512, so the increase never waits.  Each
+  // 128 x 72 + 256 x 216 = 64,512 <= 64,512, so the increase never waits.  Each
   // role's code is reachable only after its own setmaxnreg; the common tail is tiny.
   if (skip) {
     // nothing to do: fall through to the teardown
   } else if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_kv > 0) {
@@ -323,62 +323,68 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // The whole warp runs this loop in step (waits, descriptors, counters); one
+    // elected lane issues each MMA and commit.
+    if (n_kv > 0) {
+      const uint32_t is = elect_one();
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
       constexpr uint32_t idesc_s = instr_desc(BN, false);
       constexpr uint32_t idesc_pv = instr_desc(D, true);
       const uint32_t s_col[2] = {0u, 128u};
       const uint32_t o_col[2] = {K::kOCol, K::kOCol + uint32_t(D)};
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      bool ok = wait(bar_q, 0);
       auto issue_s = [&](int tt, int slot) {
         const uint32_t qa = sbase + K::kQOff + tt * K::kTileBytes;
         const uint32_t ka = sbase + K::kKvOff + slot * K::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * K::kSlab + (kk % 4) * 32;
-          mma_ss(tmem + s_col[tt], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
+          mma_ss_if(is, tmem + s_col[tt], smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int tt, int slot, bool accumulate) {
         const uint32_t va = sbase + K::kKvOff + slot * K::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem + o_col[tt], tmem + s_col[tt] + uint32_t(kk * 8), smem_desc(va + kk * 2048, K::kSlab, 1024),
-                 idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts_if(is, tmem + o_col[tt], tmem + s_col[tt] + uint32_t(kk * 8),
+                    smem_desc(va + kk * 2048, K::kSlab, 1024), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
       // prologue: S(0) for both tiles
-      if (ok) ok = mbar_wait(bar_full(0), 0, abort_flag);
+      if (ok) ok = wait(bar_full(0), 0);
       if (ok) {
         tc_fence_after();
         for (int tt = 0; tt < n_q; ++tt) {
           issue_s(tt, 0);
-          mma_commit(bar_s(tt));
+          mma_commit_if(is, bar_s(tt));
         }
-        mma_commit(bar_empty(0));
+        mma_commit_if(is, bar_empty(0));
       }
       for (int32_t j = 0; ok && j < n_kv; ++j) {
         const int lv = 2 * j + 1, lk = 2 * j + 2;
         const int sv = lv % K::kStages, sk = lk % K::kStages;
-        if (!mbar_wait(bar_full(sv), uint32_t((lv / K::kStages) & 1), abort_flag)) { ok = false; break; }
+        if (!wait(bar_full(sv), uint32_t((lv / K::kStages) & 1))) { ok = false; break; }
         const bool more = (j + 1 < n_kv);
         bool k_ready = false;
         for (int tt = 0; tt < n_q; ++tt) {
-          if (!mbar_wait(bar_p(tt), uint32_t(j & 1), abort_flag)) { ok = false; break; }
+          if (!wait(bar_p(tt), uint32_t(j & 1))) { ok = false; break; }
           tc_fence_after();
           issue_pv(tt, sv, j > 0);
-          if (tt == n_q - 1) mma_commit(bar_empty(sv));  // V_j consumed by every tile
+          if (tt == n_q - 1) mma_commit_if(is, bar_empty(sv));  // V_j consumed by every tile
           if (more) {
             if (!k_ready) {
-              if (!mbar_wait(bar_full(sk), uint32_t((lk / K::kStages) & 1), abort_flag)) { ok = false; break; }
+              if (!wait(bar_full(sk), uint32_t((lk / K::kStages) & 1))) { ok = false; break; }
               tc_fence_after();
               k_ready = true;
             }
             issue_s(tt, sk);
-            mma_commit(bar_s(tt));
-            if (tt == n_q - 1) mma_commit(bar_empty(sk));  // K_{j+1} consumed
+            mma_commit_if(is, bar_s(tt));
+            if (tt == n_q - 1) mma_commit_if(is, bar_empty(sk));  // K_{j+1} consumed
           } else {
-            mma_commit(bar_o(tt));
+            mma_commit_if(is, bar_o(tt));
           }
         }
       }
