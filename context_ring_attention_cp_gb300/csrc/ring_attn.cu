@@ -166,6 +166,28 @@ struct KvCursor {
     }
   }
 
+  // Number of tiles next() yields over [t0, t1): the same segments, counted per
+  // segment instead of per tile.
+  __device__ static int32_t count(int32_t cp, int32_t r, int32_t c_q, int32_t t0, int32_t t1, int32_t C,
+                                  int32_t q_last) {
+    const int32_t full = (C + BN - 1) / BN;
+    int32_t n = 0;
+    int32_t s = ((r - t0) % cp + cp) % cp;
+    for (int32_t t = t0; t < t1; ++t) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int32_t c = (LAYOUT == CP_LAYOUT_SEQUENTIAL) ? (2 * s + half) : ((half == 0) ? s : 2 * cp - 1 - s);
+        if (c < c_q) {
+          n += full;
+        } else if (c == c_q) {
+          n += (q_last - c * C) / BN + 1;
+        }
+      }
+      s = (s == 0) ? cp - 1 : s - 1;
+    }
+    return n;
+  }
+
   __device__ bool next(int32_t& key0, int32_t& key_end, bool& diag) {
     if (seg_i >= seg_n) {
       find();
@@ -266,16 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
-
   // Number of KV tiles this query tile visits over the step range.
-  int32_t n_kv = 0;
-  {
-    KvCursor<LAYOUT> cur;
-    cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
-    int32_t k0, ke;
-    bool dg;
-    while (cur.next(k0, ke, dg)) ++n_kv;
-  }
+  const int32_t n_kv = KvCursor<LAYOUT>::count(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C,
+                                               it.q_row0 + it.q_rows - 1);
   const int n_q = 1 + it.has_b;
 
   // Register split (launched with 168 per thread, 64,512 in all): the producer /
