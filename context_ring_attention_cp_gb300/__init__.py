@@ -21,6 +21,7 @@ import numpy as np
 __all__ = [
     "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE",
     "CP_MAX_MERGE_PARTS", "library_path", "load_library", "cp_status_string",
+    "cp_ring_attn_host", "cp_ring_attn_host_workspace_bytes",
     "cp_plan_balanced_chunks", "cp_plan_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn",
     "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
@@ -104,6 +105,8 @@ def load_library():
                                           _I32, _P]),
         "cp_passq_decode_noalloc": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P]),
         "cp_selftest_wait_timeout": (_I32, [_P]),
+        "cp_ring_attn_host_workspace_bytes": (_I32, [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]),
+        "cp_ring_attn_host": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -198,6 +201,27 @@ def cp_ring_rank_partial_attn(desc: AttnDesc, layout: int, rank_begin: int, rank
                                        int(step_begin), int(step_end), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m),
                                        _ptr(l), int(mode), _stream(stream))
     _check(st, "cp_ring_rank_partial_attn")
+
+
+def cp_ring_attn_host_workspace_bytes(desc: AttnDesc) -> int:
+    """Bytes of device workspace cp_ring_attn_host needs for ``desc``."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().cp_ring_attn_host_workspace_bytes(ctypes.byref(desc), ctypes.byref(n)),
+           "cp_ring_attn_host_workspace_bytes")
+    return int(n.value)
+
+
+def cp_ring_attn_host(desc: AttnDesc, q_host, k_host, v_host, o_host, m_host, l_host, workspace,
+                      workspace_bytes: int, stream=None) -> None:
+    """The full balanced ring (EMIT | FINALIZE) on host tensors, copies overlapped with compute.
+
+    The host tensors are CPU tensors (pinned for overlap); ``workspace`` is a device buffer of at
+    least cp_ring_attn_host_workspace_bytes(desc) bytes.  Asynchronous on ``stream``.
+    """
+    lib = load_library()
+    st = lib.cp_ring_attn_host(ctypes.byref(desc), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host),
+                               _ptr(m_host), _ptr(l_host), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "cp_ring_attn_host")
 
 
 def cp_merge_partials(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out,

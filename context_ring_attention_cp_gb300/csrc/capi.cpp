@@ -11,6 +11,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 using namespace cpattn;
@@ -51,6 +53,68 @@ cudaError_t current_sm_count(int* sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer ring: device workspace layout and the pipeline's streams
+// ---------------------------------------------------------------------------
+
+constexpr size_t kWsAlign = 256;
+size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+struct HostRingLayout {
+  size_t q, k, v, o, m, l;  // byte offsets into the workspace
+  size_t total;
+};
+
+HostRingLayout host_ring_layout(const cp_attn_desc& d) {
+  HostRingLayout w;
+  const size_t qb = size_t(d.b) * d.S * d.h_q * d.d * 2;
+  const size_t kb = size_t(d.b) * d.S * d.h_kv * d.d * 2;
+  const size_t ob = size_t(d.b) * d.S * d.h_q * d.d * 4;
+  const size_t mb = size_t(d.b) * d.h_q * d.S * 4;
+  w.q = 0;
+  w.k = w.q + round_up(qb);
+  w.v = w.k + round_up(kb);
+  w.o = w.v + round_up(kb);
+  w.m = w.o + round_up(ob);
+  w.l = w.m + round_up(mb);
+  w.total = w.l + round_up(mb);
+  return w;
+}
+
+cp_status check_host_ring(const cp_attn_desc* desc) {
+  cp_status st = check_desc_common(desc);
+  if (st != CP_OK) return st;
+  if (desc->S % (2 * desc->cp) != 0) return CP_ERR_INVALID_ARGUMENT;
+  if (desc->causal != 1) return CP_ERR_UNSUPPORTED;
+  if (!ring_supported(*desc)) return CP_ERR_UNSUPPORTED;
+  return CP_OK;
+}
+
+struct PipeStreams {
+  cudaStream_t in, comp[2], out;
+};
+
+// Created on first use per device and kept for the life of the process.
+bool pipe_streams(PipeStreams* out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static PipeStreams per_dev[kMaxDev];
+  static bool made[kMaxDev] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!made[dev]) {
+    PipeStreams s;
+    cudaStream_t* all[4] = {&s.in, &s.comp[0], &s.comp[1], &s.out};
+    for (cudaStream_t* x : all)
+      if (cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) != cudaSuccess) return false;
+    per_dev[dev] = s;
+    made[dev] = true;
+  }
+  *out = per_dev[dev];
+  return true;
 }
 
 }  // namespace
@@ -167,6 +231,131 @@ cp_status cp_ring_step_partial_attn(const cp_attn_desc* desc, int32_t step_begin
   if (desc->cp < 1 || desc->cp > (1 << 20)) return CP_ERR_INVALID_ARGUMENT;
   return cp_ring_rank_partial_attn(desc, CP_LAYOUT_BALANCED, 0, int32_t(desc->cp), step_begin, step_end, q, k, v,
                                    o, m, l, mode, cuda_stream);
+}
+
+cp_status cp_ring_attn_host_workspace_bytes(const cp_attn_desc* desc, size_t* bytes) {
+  cp_status st = check_host_ring(desc);
+  if (st != CP_OK) return st;
+  if (bytes == nullptr) return CP_ERR_INVALID_ARGUMENT;
+  *bytes = host_ring_layout(*desc).total;
+  return CP_OK;
+}
+
+cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const void* k_host, const void* v_host,
+                            float* o_host, float* m_host, float* l_host, void* workspace, size_t workspace_bytes,
+                            void* cuda_stream) {
+  cp_status st = check_host_ring(desc);
+  if (st != CP_OK) return st;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || o_host == nullptr || m_host == nullptr ||
+      l_host == nullptr)
+    return CP_ERR_INVALID_ARGUMENT;
+  const HostRingLayout w = host_ring_layout(*desc);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0 || workspace_bytes < w.total)
+    return CP_ERR_INVALID_ARGUMENT;
+  PipeStreams ps;
+  if (!pipe_streams(&ps)) return CP_ERR_CUDA;
+
+  const cp_attn_desc& d = *desc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* dq = ws + w.q;
+  void* dk = ws + w.k;
+  void* dv = ws + w.v;
+  float* dout = reinterpret_cast<float*>(ws + w.o);
+  float* dm = reinterpret_cast<float*>(ws + w.m);
+  float* dl = reinterpret_cast<float*>(ws + w.l);
+  const int32_t cp = int32_t(d.cp);
+  const int64_t C = d.S / (2 * d.cp);
+  const int32_t n_groups = cp < 8 ? cp : 8;
+  const size_t q_row = size_t(d.h_q) * d.d * 2;  // bytes of one token's Q
+  const size_t o_row = size_t(d.h_q) * d.d * 4;
+  const size_t kv_bytes = size_t(d.b) * d.S * d.h_kv * d.d * 2;
+  cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
+
+  constexpr int kMaxEv = 6 + 2 * 8;
+  cudaEvent_t ev[kMaxEv];
+  int n_ev = 0;
+  bool ok = true;
+  for (int i = 0; i < 6 + 2 * n_groups && ok; ++i, ++n_ev)
+    ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    for (int i = 0; i + 1 < n_ev; ++i) cudaEventDestroy(ev[i]);
+    return CP_ERR_CUDA;
+  }
+  cudaEvent_t e_start = ev[0], e_kv = ev[1], e_done = ev[2];
+  cudaEvent_t e_tail[3] = {ev[3], ev[4], ev[5]};  // end of the in / compute streams' work
+  auto e_q = [&](int g) { return ev[6 + g]; };
+  auto e_c = [&](int g) { return ev[6 + n_groups + g]; };
+  auto chk = [&](cudaError_t e) {
+    if (e != cudaSuccess) ok = false;
+  };
+  // Rank group g: ranks [r0, r1) own chunks [r0, r1) and [2cp - r1, 2cp - r0).
+  auto group_ranks = [&](int g, int32_t* r0, int32_t* r1) {
+    *r0 = int32_t(int64_t(g) * cp / n_groups);
+    *r1 = int32_t(int64_t(g + 1) * cp / n_groups);
+  };
+  // One contiguous range of chunks [c0, c1) of a [b, S, ...] tensor (row bytes given)
+  // or of a [b, h, S] fp32 tensor: per-batch (or per-(batch, head)) strided copies.
+  auto copy_tok = [&](void* dst, const void* src, int64_t c0, int64_t c1, size_t row, cudaMemcpyKind kind,
+                      cudaStream_t s) {
+    const size_t off = size_t(c0 * C) * row;
+    chk(cudaMemcpy2DAsync(static_cast<uint8_t*>(dst) + off, size_t(d.S) * row,
+                          static_cast<const uint8_t*>(src) + off, size_t(d.S) * row, size_t((c1 - c0) * C) * row,
+                          size_t(d.b), kind, s));
+  };
+  auto copy_ml = [&](float* dst, const float* src, int64_t c0, int64_t c1, cudaStream_t s) {
+    chk(cudaMemcpy2DAsync(dst + c0 * C, size_t(d.S) * 4, src + c0 * C, size_t(d.S) * 4, size_t((c1 - c0) * C) * 4,
+                          size_t(d.b * d.h_q), cudaMemcpyDeviceToHost, s));
+  };
+
+  chk(cudaEventRecord(e_start, caller));
+  chk(cudaStreamWaitEvent(ps.in, e_start, 0));
+  chk(cudaStreamWaitEvent(ps.comp[0], e_start, 0));
+  chk(cudaStreamWaitEvent(ps.comp[1], e_start, 0));
+  chk(cudaStreamWaitEvent(ps.out, e_start, 0));
+  chk(cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, ps.in));
+  chk(cudaMemcpyAsync(dv, v_host, kv_bytes, cudaMemcpyHostToDevice, ps.in));
+  chk(cudaEventRecord(e_kv, ps.in));
+  for (int g = 0; g < n_groups && ok; ++g) {
+    int32_t r0, r1;
+    group_ranks(g, &r0, &r1);
+    copy_tok(dq, q_host, r0, r1, q_row, cudaMemcpyHostToDevice, ps.in);
+    copy_tok(dq, q_host, 2 * cp - r1, 2 * cp - r0, q_row, cudaMemcpyHostToDevice, ps.in);
+    chk(cudaEventRecord(e_q(g), ps.in));
+  }
+  for (int g = 0; g < n_groups && ok; ++g) {
+    int32_t r0, r1;
+    group_ranks(g, &r0, &r1);
+    cudaStream_t cs = ps.comp[g & 1];
+    chk(cudaStreamWaitEvent(cs, e_kv, 0));
+    chk(cudaStreamWaitEvent(cs, e_q(g), 0));
+    if (!ok) break;
+    st = launch_ring_attn(d, CP_LAYOUT_BALANCED, r0, r1, 0, cp, dq, dk, dv, dout, dm, dl,
+                          CP_MODE_EMIT | CP_MODE_FINALIZE, cs);
+    if (st != CP_OK) {
+      ok = false;
+      break;
+    }
+    chk(cudaEventRecord(e_c(g), cs));
+    chk(cudaStreamWaitEvent(ps.out, e_c(g), 0));
+    copy_tok(o_host, dout, r0, r1, o_row, cudaMemcpyDeviceToHost, ps.out);
+    copy_tok(o_host, dout, 2 * cp - r1, 2 * cp - r0, o_row, cudaMemcpyDeviceToHost, ps.out);
+    copy_ml(m_host, dm, r0, r1, ps.out);
+    copy_ml(m_host, dm, 2 * cp - r1, 2 * cp - r0, ps.out);
+    copy_ml(l_host, dl, r0, r1, ps.out);
+    copy_ml(l_host, dl, 2 * cp - r1, 2 * cp - r0, ps.out);
+  }
+  // Whatever was queued (also after a failure part-way), the caller's stream waits
+  // for all of it, so no copy still reads or writes the caller's buffers afterwards.
+  cudaStream_t others[3] = {ps.in, ps.comp[0], ps.comp[1]};
+  for (int i = 0; i < 3; ++i) {
+    cudaEventRecord(e_tail[i], others[i]);
+    cudaStreamWaitEvent(ps.out, e_tail[i], 0);
+  }
+  cudaEventRecord(e_done, ps.out);
+  cudaStreamWaitEvent(caller, e_done, 0);
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+  if (!ok) return st != CP_OK ? st : CP_ERR_CUDA;
+  return CP_OK;
 }
 
 cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t d,

@@ -149,6 +149,36 @@ CPATTN_API cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t
                                                float* l, int32_t mode, void* cuda_stream);
 
 /*
+ * The whole balanced ring for tensors held in HOST memory, with the host<->device
+ * copies overlapped with the computation inside the call.  The operation is
+ * cp_ring_step_partial_attn over all cp steps in EMIT | FINALIZE mode (Terms table
+ * rows "Balanced chunk split", "Pass-KV", "Ring step" and "Partial attention"):
+ *   q_host [b, S, h_q, d] bf16, k_host / v_host [b, S, h_kv, d] bf16 (read);
+ *   o_host [b, S, h_q, d] fp32 = O / l, m_host / l_host [b, h_q, S] fp32 (written).
+ * All six are caller-owned host memory; page-locked (pinned) memory lets the
+ * copies overlap the kernels, pageable memory gives the same results more slowly.
+ * `workspace` (device, caller-owned, 256-byte aligned, at least
+ * cp_ring_attn_host_workspace_bytes bytes) receives the device copies of all six.
+ * Pipeline: K and V are copied first (every rank's ring steps read all of them).
+ * The ranks are then taken in up to 8 groups.  A group's Q rows (its ranks' two
+ * chunks each) are copied in, one launch runs all cp ring steps for those rows, and
+ * its O, m and l rows are copied out.  Copies in, launches (two streams, so one
+ * launch's last CTAs overlap the next) and copies out run on separate streams
+ * that the library creates once per device, so one group's copies overlap other
+ * groups' computation.  The call is ordered on `cuda_stream`: it starts after the
+ * work queued there before it, later work queued there starts after its last
+ * copy, and the workspace is in use until then.  The host is not blocked:
+ * synchronise `cuda_stream` before reading the outputs.
+ * Errors: as cp_ring_step_partial_attn, plus a NULL host pointer or a misaligned
+ * or too small workspace -> CP_ERR_INVALID_ARGUMENT; a failed copy, launch or
+ * stream/event call -> CP_ERR_CUDA.
+ */
+CPATTN_API cp_status cp_ring_attn_host_workspace_bytes(const cp_attn_desc* desc, size_t* bytes);
+CPATTN_API cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const void* k_host,
+                                       const void* v_host, float* o_host, float* m_host, float* l_host,
+                                       void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * LSE merge of n_parts partial triples (Terms table, row "Partial attention":
  * the merge is associative and order-free; pass-Q paragraph of the
  * Algorithm/formulas section: the reduce carries O, the max and the denominator).

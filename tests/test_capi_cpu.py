@@ -261,3 +261,43 @@ def test_tree_merge_needs_a_power_of_two(cpa, n):
 def test_tree_merge_workspace_size(cpa):
     # two ping-pong levels of n/2 triples: O (d floats) + m + l per (part, batch, row, head)
     assert cpa.cp_merge_tree_workspace_bytes(1, 4096, 64, 128, 32) == 2 * 16 * 4096 * 64 * (128 + 2) * 4
+
+
+def _round256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_host_ring_workspace_size(cpa):
+    # device copies of q, k, v (bf16), o (fp32) and m, l (fp32), each rounded up to 256 bytes
+    b, S, hq, hkv, d = 2, 1000, 6, 2, 128
+    want = (_round256(b * S * hq * d * 2) + 2 * _round256(b * S * hkv * d * 2) + _round256(b * S * hq * d * 4)
+            + 2 * _round256(b * hq * S * 4))
+    assert cpa.cp_ring_attn_host_workspace_bytes(_desc(cpa, b=b, S=S, h_q=hq, h_kv=hkv, d=d)) == want
+
+
+@pytest.mark.parametrize("kw,status", [(dict(cp=0), 1), (dict(S=1000, cp=8), 1), (dict(h_q=6, h_kv=4), 1),
+                                       (dict(d=96), 2), (dict(causal=0), 2)])
+def test_host_ring_rejects_descriptors(cpa, kw, status):
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_attn_host_workspace_bytes(_desc(cpa, **kw))
+    assert e.value.status == status
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_attn_host(_desc(cpa, **kw), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, 1 << 40, stream=0)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("bad", range(7))
+def test_host_ring_rejects_null_pointers_and_small_or_misaligned_workspace(cpa, bad):
+    desc = _desc(cpa)
+    need = cpa.cp_ring_attn_host_workspace_bytes(desc)
+    ptrs = [FAKE] * 6 + [4096]
+    ptrs[bad] = 0
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_ring_attn_host(desc, *ptrs, need, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:  # workspace one byte short
+        cpa.cp_ring_attn_host(desc, *([FAKE] * 6), 4096, need - 1, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(cpa.CpError) as e:  # workspace not 256-byte aligned
+        cpa.cp_ring_attn_host(desc, *([FAKE] * 6), 4096 + 16, need, stream=0)
+    assert e.value.status == 1
