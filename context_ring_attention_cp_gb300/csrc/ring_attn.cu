@@ -91,6 +91,7 @@ struct RingParams {
   CUtensorMap tmap_q;  // dims (d, h_q, S, b)
   CUtensorMap tmap_k;  // dims (d, h_kv, S, b)
   CUtensorMap tmap_v;
+  CUtensorMap tmap_o;  // fp32, dims (d, h_q, S, b), box 32 x 1 x 128 x 1: O tile stores
   float* o;
   float* m;
   float* l;
@@ -257,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   auto bar_s = [&](int tt) { return smem_u32(&bars[1 + 2 * K::kStages + tt]); };
   auto bar_p = [&](int tt) { return smem_u32(&bars[3 + 2 * K::kStages + tt]); };
   auto bar_o = [&](int tt) { return smem_u32(&bars[5 + 2 * K::kStages + tt]); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[8 + 2 * K::kStages]);
+  auto bar_e = [&](int tt) { return smem_u32(&bars[7 + 2 * K::kStages + tt]); };  // O tile staged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[10 + 2 * K::kStages]);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       mbar_init(bar_s(tt), 1);
       mbar_init(bar_p(tt), BM / 32);
       mbar_init(bar_o(tt), 1);
+      mbar_init(bar_e(tt), BM / 32);
     }
     // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) ? 1 : 0;
@@ -538,33 +541,72 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const float inv = (fin && l_out > 0.f) ? 1.f / l_out : (fin ? 0.f : 1.f);
       const float wnew = beta * fre * inv;
       const float wold = alpha * inv;
-      float* orow = p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + h) * D;
+      // A whole 128-row tile written plainly goes through shared memory and TMA tile
+      // stores (128 rows x 32 floats a box); partial tiles and ACCUMULATE store
+      // each row directly.  Staging: tile A uses the Q tiles' space, tile B two K/V
+      // slots; every MMA that read them has completed once bar_o(tt) has fired.
+      const bool staged = !(p.mode & CP_MODE_ACCUMULATE) && it.q_rows == BM && it.q_row0 + BM <= p.S;
+      if (staged) {
+        const uint32_t stage = sbase + (tt == 0 ? uint32_t(K::kQOff) : uint32_t(K::kKvOff));
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        if (have) {
-          tmem_ld32(o_addr + uint32_t(c * 32), r);
-          tmem_ld_wait(r);
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          if (have) {
+            tmem_ld32(o_addr + uint32_t(c * 32), r);
+            tmem_ld_wait(r);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          // box c, row t, 16-byte chunk k at position k ^ (t % 8) (128-byte swizzle)
+          const uint32_t rowa = stage + uint32_t(c * BM * 128 + t * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_shared_v4(rowa + uint32_t(((k ^ (t & 7)) << 4)), __uint_as_float(r[4 * k]) * wnew,
+                         __uint_as_float(r[4 * k + 1]) * wnew, __uint_as_float(r[4 * k + 2]) * wnew,
+                         __uint_as_float(r[4 * k + 3]) * wnew);
         }
-        if (row_ok) {
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_e(tt));
+        if (warp == 4 + 4 * tt && lane == 0) {
+          if (mbar_wait(bar_e(tt), 0, abort_flag)) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v;
-            v.x = __uint_as_float(r[i]) * wnew;
-            v.y = __uint_as_float(r[i + 1]) * wnew;
-            v.z = __uint_as_float(r[i + 2]) * wnew;
-            v.w = __uint_as_float(r[i + 3]) * wnew;
-            if (p.mode & CP_MODE_ACCUMULATE) {
-              const float4 old = *reinterpret_cast<const float4*>(orow + c * 32 + i);
-              v.x = fmaf(old.x, wold, v.x);
-              v.y = fmaf(old.y, wold, v.y);
-              v.z = fmaf(old.z, wold, v.z);
-              v.w = fmaf(old.w, wold, v.w);
+            for (int c = 0; c < D / 32; ++c)
+              tma_store_4d(&p.tmap_o, stage + uint32_t(c * BM * 128), c * 32, h, it.q_row0, it.bi);
+            bulk_commit();
+            bulk_wait_all();
+          }
+        }
+      } else {
+        float* orow = p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          if (have) {
+            tmem_ld32(o_addr + uint32_t(c * 32), r);
+            tmem_ld_wait(r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 v;
+              v.x = __uint_as_float(r[i]) * wnew;
+              v.y = __uint_as_float(r[i + 1]) * wnew;
+              v.z = __uint_as_float(r[i + 2]) * wnew;
+              v.w = __uint_as_float(r[i + 3]) * wnew;
+              if (p.mode & CP_MODE_ACCUMULATE) {
+                const float4 old = *reinterpret_cast<const float4*>(orow + c * 32 + i);
+                v.x = fmaf(old.x, wold, v.x);
+                v.y = fmaf(old.y, wold, v.y);
+                v.z = fmaf(old.z, wold, v.z);
+                v.w = fmaf(old.w, wold, v.w);
+              }
+              *reinterpret_cast<float4*>(orow + c * 32 + i) = v;
             }
-            *reinterpret_cast<float4*>(orow + c * 32 + i) = v;
           }
         }
       }
@@ -621,6 +663,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 // 4-D bf16 map over a [b, S, h, d] tensor: dims (d, h, S, b), box (64, 1, 128, 1), 128-byte swizzle.
+// 4-D fp32 map over the [b, S, h, d] output: box (32, 1, 128, 1), 128-byte swizzle.
+bool encode_map_o(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_t h, int64_t d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(h), cuuint64_t(S), cuuint64_t(b)};
+  const cuuint64_t strides[3] = {cuuint64_t(d * 4), cuuint64_t(h * d * 4), cuuint64_t(S * h * d * 4)};
+  const cuuint32_t box[4] = {32, 1, BM, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_t h, int64_t d) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
   if (enc == nullptr) return false;
@@ -657,7 +713,7 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   RingParams p;
   memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tmap_q, q, d.b, d.S, d.h_q, d.d) || !encode_map(&p.tmap_k, k, d.b, d.S, d.h_kv, d.d) ||
-      !encode_map(&p.tmap_v, v, d.b, d.S, d.h_kv, d.d))
+      !encode_map(&p.tmap_v, v, d.b, d.S, d.h_kv, d.d) || !encode_map_o(&p.tmap_o, o, d.b, d.S, d.h_q, d.d))
     return CP_ERR_CUDA;
   p.o = o;
   p.m = m;
