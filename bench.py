@@ -564,6 +564,15 @@ def profile_case(name, steps):
         out = torch.empty((b, h, d), dtype=torch.float32, device="cuda")
         fn = lambda: cpa.cp_passq_decode(desc, q, k, v, ws, nbytes, out, None, None, stream)  # noqa: E731
         work = 2 * b * L * h * d * 2
+    elif name == "decode-shared-kv":  # b8, 16 q heads on one 512-wide K/V head, L131072, cp8: 2.1 GB
+        b, L, hq, hkv, d, cp = 8, 131072, 16, 1, 512, 8
+        q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=7)
+        desc = cpa.make_desc(b, L, hq, hkv, d, cp, 1.0 / math.sqrt(d), 0)
+        nbytes = cpa.cp_passq_workspace_bytes(desc)
+        ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+        fn = lambda: cpa.cp_passq_decode(desc, q, k, v, ws, nbytes, out, None, None, stream)  # noqa: E731
+        work = 2 * b * L * hkv * d * 2
     elif name == "merge":  # the merge-stress workload itself: 4.5 GB
         w = synth.WORKLOADS["merge"]
         po, pm, pl = synth.merge_parts(w["parts"], w["heads"], w["rows"], w["d"], spread=w["spread"], seed=w["seed"])
@@ -592,7 +601,7 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--case", choices=["decode-small", "merge"], default=None,
+    ap.add_argument("--case", choices=["decode-small", "decode-shared-kv", "merge"], default=None,
                     help="time one kernel on a capture-sized case (for ncu) instead of the benchmark")
     args = ap.parse_args()
     if args.case is not None:

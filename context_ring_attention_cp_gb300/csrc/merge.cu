@@ -143,14 +143,20 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(c
   }
 }
 
-// rows == 1 (the decode reduce: one triple per sequence and head): one CTA per
-// (batch, head).  The part weights e^{m_p - m} are computed once into shared
-// memory, then each thread streams a float4 slice of d through every part in the
-// caller's order.
-__global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_constant__ MergeParams p) {
-  extern __shared__ float smem[];
-  float* w = smem;                             // [n_parts] weights in fold order
-  float* red = smem + CP_MAX_MERGE_PARTS;      // [kWarps] partial maxima / sums
+// rows == 1 (the decode reduce: one triple per sequence and head).  One CTA per
+// (batch, head, slice of 128 columns), so the grid has batch * heads * ceil(d/128)
+// CTAs.  The part weights e^{m_p - m} are computed once into shared memory.  Each
+// of the four warps then folds a contiguous quarter of the parts, in the caller's
+// order, into one float4 column per lane with eight loads in flight; the quarters
+// are added in order.
+constexpr int kR1Threads = 128;
+constexpr int kR1Warps = kR1Threads / 32;
+constexpr int kR1SliceVec = 32;  // float4 columns per CTA: 128 floats
+
+__global__ void __launch_bounds__(kR1Threads) lse_merge_rows1_kernel(const __grid_constant__ MergeParams p) {
+  __shared__ float w[CP_MAX_MERGE_PARTS];  // weights in fold order
+  __shared__ float red[kR1Warps];          // partial maxima / sums
+  __shared__ float4 part_sum[kR1Warps][kR1SliceVec];
   const int n = p.n_parts;
   const int64_t bh = blockIdx.x;
   const int64_t h = bh % p.heads, bi = bh / p.heads;
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
   auto ml_off = [&](int part) { return (int64_t(part) * p.batch + bi) * p.heads + h; };  // rows == 1
 
   float mx = -INFINITY;
-  for (int k = threadIdx.x; k < n; k += kThreads) {
+  for (int k = threadIdx.x; k < n; k += kR1Threads) {
     const float m = p.m_parts[ml_off(p.order[k])];
     w[k] = m;
     mx = fmaxf(mx, m);
@@ -169,11 +175,11 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
   __syncthreads();
   mx = red[0];
 #pragma unroll
-  for (int i = 1; i < kWarps; ++i) mx = fmaxf(mx, red[i]);
+  for (int i = 1; i < kR1Warps; ++i) mx = fmaxf(mx, red[i]);
   const float shift = (mx == -INFINITY) ? 0.f : mx;  // all parts the identity: stays the identity
   __syncthreads();
   float ls = 0.f;
-  for (int k = threadIdx.x; k < n; k += kThreads) {
+  for (int k = threadIdx.x; k < n; k += kR1Threads) {
     const float wk = expf(w[k] - shift);
     w[k] = wk;
     ls = fmaf(wk, p.l_parts[ml_off(p.order[k])], ls);
@@ -184,23 +190,25 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
   __syncthreads();
   float lsum = 0.f;
 #pragma unroll
-  for (int i = 0; i < kWarps; ++i) lsum += red[i];
+  for (int i = 0; i < kR1Warps; ++i) lsum += red[i];
 
   const int64_t n_vec = p.d / 4;
+  const int64_t c = int64_t(blockIdx.y) * kR1SliceVec + lane;  // this lane's float4 column
+  const bool col_ok = c < n_vec;
   const int64_t part_stride = p.batch * p.heads * p.d;  // rows == 1
   const int64_t obase = (bi * p.heads + h) * p.d;
-  const float inv = (p.finalize && lsum > 0.f) ? 1.f / lsum : 1.f;
-  const bool zero = p.finalize && !(lsum > 0.f);
-  for (int64_t c = threadIdx.x; c < n_vec; c += kThreads) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = 0;
-    for (; k + 4 <= n; k += 4) {
-      float4 x[4];
+  const int k_begin = int(int64_t(n) * warp / kR1Warps);
+  const int k_end = int(int64_t(n) * (warp + 1) / kR1Warps);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col_ok) {
+    int k = k_begin;
+    for (; k + 8 <= k_end; k += 8) {
+      float4 x[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
         x[u] = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(p.order[k + u]) * part_stride + obase) + c);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const float wk = w[k + u];
         acc.x = fmaf(wk, x[u].x, acc.x);
         acc.y = fmaf(wk, x[u].y, acc.y);
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
         acc.w = fmaf(wk, x[u].w, acc.w);
       }
     }
-    for (; k < n; ++k) {
+    for (; k < k_end; ++k) {
       const float4 x = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(p.order[k]) * part_stride + obase) + c);
       const float wk = w[k];
       acc.x = fmaf(wk, x.x, acc.x);
@@ -216,14 +224,29 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
       acc.z = fmaf(wk, x.z, acc.z);
       acc.w = fmaf(wk, x.w, acc.w);
     }
-    if (zero) {
-      acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else if (p.finalize) {
-      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-    }
-    reinterpret_cast<float4*>(p.o_out + obase)[c] = acc;
   }
-  if (threadIdx.x == 0) {
+  part_sum[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && col_ok) {
+    float4 o = part_sum[0][lane];
+#pragma unroll
+    for (int i = 1; i < kR1Warps; ++i) {
+      const float4 q = part_sum[i][lane];
+      o.x += q.x;
+      o.y += q.y;
+      o.z += q.z;
+      o.w += q.w;
+    }
+    if (p.finalize) {
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;  // no visible key at all: output 0
+      o.x *= inv;
+      o.y *= inv;
+      o.z *= inv;
+      o.w *= inv;
+    }
+    reinterpret_cast<float4*>(p.o_out + obase)[c] = o;
+  }
+  if (threadIdx.x == 0 && blockIdx.y == 0) {
     if (p.m_out) p.m_out[bi * p.heads + h] = mx;
     if (p.l_out) p.l_out[bi * p.heads + h] = lsum;
   }
@@ -234,9 +257,9 @@ __global__ void __launch_bounds__(kThreads) lse_merge_rows1_kernel(const __grid_
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.rows == 1) {
     const int64_t ctas = p.batch * p.heads;
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const size_t smem = (CP_MAX_MERGE_PARTS + kWarps) * sizeof(float);
-    lse_merge_rows1_kernel<<<unsigned(ctas), kThreads, smem, stream>>>(p);
+    const int64_t slices = (p.d / 4 + kR1SliceVec - 1) / kR1SliceVec;
+    if (ctas > 0x7fffffffLL || slices > 65535) return cudaErrorInvalidValue;
+    lse_merge_rows1_kernel<<<dim3(unsigned(ctas), unsigned(slices)), kR1Threads, 0, stream>>>(p);
     return cudaGetLastError();
   }
   const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
