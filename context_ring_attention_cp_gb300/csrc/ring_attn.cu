@@ -479,20 +479,21 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       float ps8[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) ps8[a] = 0.f;
+      // All 64 packed columns of P go back in one TMEM store (fewer store instructions
+      // measured faster than four or eight smaller ones).
+      {
+        uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 64; ++i) {
           float ya, yb;
-          fma2(ya, yb, x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1], p.sl, p.sl, nmu, nmu);
+          fma2(ya, yb, x[2 * i], x[2 * i + 1], p.sl, p.sl, nmu, nmu);
           const float a = ex2(ya);
           const float b = ex2(yb);
           const int acc = (2 * i) % 8;
           add2(ps8[acc], ps8[acc + 1], ps8[acc], ps8[acc + 1], a, b);
           pk[i] = pack_bf16(a, b);
         }
-        tmem_st32(s_addr + uint32_t(c * 32), pk);
+        tmem_st64(s_addr, pk);
       }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       // O is rescaled after P is out (the logits are dead by then); PV_T(j)
