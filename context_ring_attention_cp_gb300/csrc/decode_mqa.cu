@@ -95,6 +95,13 @@ struct MqaParams {
   float sl;         // scale * log2(e)
 };
 
+// Maximum over the warp's 32 lanes in one instruction.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_constant__ MqaParams p) {
   using K = MqaCfg<D, G>;
@@ -109,10 +116,12 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
   auto bar_empty = [&](int s) { return smem_u32(&bars[4 + K::kSlots + s]); };
   auto bar_s = [&](int b) { return smem_u32(&bars[4 + 2 * K::kSlots + b]); };
   auto bar_p = [&](int b) { return smem_u32(&bars[6 + 2 * K::kSlots + b]); };
-  const uint32_t bar_o = smem_u32(&bars[8 + 2 * K::kSlots]);      // O^T of a tile complete
-  const uint32_t bar_of = smem_u32(&bars[9 + 2 * K::kSlots]);     // O^T read by the epilogue
-  const uint32_t bar_red = smem_u32(&bars[10 + 2 * K::kSlots]);   // the four softmax warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[11 + 2 * K::kSlots]);
+  // O^T of tile t complete: barrier t % 2 (phase t / 2), so a wait for tile t - 2 is never
+  // ambiguous (tile t cannot complete before this softmax writes P(t)).
+  auto bar_o = [&](int32_t t) { return smem_u32(&bars[8 + 2 * K::kSlots + (t & 1)]); };
+  const uint32_t bar_of = smem_u32(&bars[10 + 2 * K::kSlots]);    // O^T read by the epilogue
+  const uint32_t bar_red = smem_u32(&bars[11 + 2 * K::kSlots]);   // the four softmax warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[12 + 2 * K::kSlots]);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(smem + K::kRedOff);  // [2][4][G] maxima
   float* red_l = red + 2 * 4 * G;                             // [4][G] row sums
@@ -134,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    mbar_init(bar_o, 1);
+    mbar_init(bar_o(0), 1);
+    mbar_init(bar_o(1), 1);
     mbar_init(bar_of, 4);
     mbar_init(bar_red, 4);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_mqa_status) != 0) ? 1 : 0;
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
           tc_fence_after();
           issue_o(t, j == 0);
           if (!ok) break;
-          mma_commit(bar_o);
+          mma_commit(bar_o(t));
         }
         jt += n_tiles;
       }
@@ -312,10 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
           mx[h] = x[h];
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-          for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
-        }
+        for (int h = 0; h < G; ++h) mx[h] = warp_max(mx[h]);
         // Cross-warp maxima through shared memory, double-buffered by phase; the
         // barrier is an mbarrier (bounded wait), not bar.sync, so a warp that gave
         // up cannot leave the others waiting forever.
@@ -343,10 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
             m_ref[h] = tmax;
           }
         }
-        // O^T of the previous tile complete before it is rescaled and before P buffer
-        // t % 2 (read by tile t - 2) is rewritten; at an item's first tile the previous
-        // item's epilogue already waited for it.
-        if (j > 0 && !__all_sync(0xffffffffu, wait(bar_o, uint32_t((t - 1) & 1)))) { ok = false; break; }
+        // P buffer t % 2 was last read by O^T(t - 2): that must be complete before it is
+        // rewritten (within an item's first two tiles the previous item's epilogue has
+        // already waited for it).  A rescale of O^T also needs O^T(t - 1) complete.
+        if (j >= 2 && !__all_sync(0xffffffffu, wait(bar_o(t - 2), uint32_t(((t - 2) >> 1) & 1)))) {
+          ok = false;
+          break;
+        }
+        if (any_raise && !__all_sync(0xffffffffu, wait(bar_o(t - 1), uint32_t(((t - 1) >> 1) & 1)))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         if (any_raise) {  // identical in every thread: decided from the shared maxima
 #pragma unroll
@@ -388,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
 
       // ---------------- epilogue: this item's partial triple per query head
       const int32_t t_last = jt + n_tiles - 1;
-      if (!__all_sync(0xffffffffu, wait(bar_o, uint32_t(t_last & 1)))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait(bar_o(t_last), uint32_t((t_last >> 1) & 1)))) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
