@@ -265,36 +265,55 @@ cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const 
   float* dl = reinterpret_cast<float*>(ws + w.l);
   const int32_t cp = int32_t(d.cp);
   const int64_t C = d.S / (2 * d.cp);
-  const int32_t n_groups = cp < 8 ? cp : 8;
-  const size_t q_row = size_t(d.h_q) * d.d * 2;  // bytes of one token's Q
+  const size_t q_row = size_t(d.h_q) * d.d * 2;   // bytes of one token's Q
+  const size_t kv_row = size_t(d.h_kv) * d.d * 2;
   const size_t o_row = size_t(d.h_q) * d.d * 4;
-  const size_t kv_bytes = size_t(d.b) * d.S * d.h_kv * d.d * 2;
   cudaStream_t caller = static_cast<cudaStream_t>(cuda_stream);
 
-  constexpr int kMaxEv = 6 + 2 * 8;
+  // Work units in launch order: head chunks in ascending order (head chunk c sees
+  // keys [0, (c+1) C) only, so the first can start once the first K/V chunks are in),
+  // then tail chunks in descending order (they need all of K/V, which has arrived by
+  // then).  Each unit is a contiguous range of ranks with one chunk selector.
+  const int32_t n_half = cp < 8 ? cp : 8;
+  const int32_t n_units = 2 * n_half;
+  auto unit_ranks = [&](int u, int32_t* r0, int32_t* r1) {
+    const int g = u % n_half;
+    *r0 = int32_t(int64_t(g) * cp / n_half);
+    *r1 = int32_t(int64_t(g + 1) * cp / n_half);
+  };
+  // chunk range [c0, c1) of unit u
+  auto unit_chunks = [&](int u, int64_t* c0, int64_t* c1) {
+    int32_t r0, r1;
+    unit_ranks(u, &r0, &r1);
+    if (u < n_half) {
+      *c0 = r0;
+      *c1 = r1;
+    } else {
+      *c0 = 2 * cp - r1;
+      *c1 = 2 * cp - r0;
+    }
+  };
+
+  constexpr int kMaxEv = 6 + 2 * 16 + 8 + 1;  // fixed, per unit (q, compute), K/V prefixes
   cudaEvent_t ev[kMaxEv];
+  const int n_need = 6 + 2 * n_units + n_half + 1;
   int n_ev = 0;
   bool ok = true;
-  for (int i = 0; i < 6 + 2 * n_groups && ok; ++i, ++n_ev)
+  for (int i = 0; i < n_need && ok; ++i, ++n_ev)
     ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     for (int i = 0; i + 1 < n_ev; ++i) cudaEventDestroy(ev[i]);
     return CP_ERR_CUDA;
   }
-  cudaEvent_t e_start = ev[0], e_kv = ev[1], e_done = ev[2];
-  cudaEvent_t e_tail[3] = {ev[3], ev[4], ev[5]};  // end of the in / compute streams' work
-  auto e_q = [&](int g) { return ev[6 + g]; };
-  auto e_c = [&](int g) { return ev[6 + n_groups + g]; };
+  cudaEvent_t e_start = ev[0], e_done = ev[1];
+  cudaEvent_t e_tail[3] = {ev[2], ev[3], ev[4]};  // end of the in / compute streams' work
+  auto e_q = [&](int u) { return ev[6 + u]; };
+  auto e_c = [&](int u) { return ev[6 + n_units + u]; };
+  auto e_kv = [&](int g) { return ev[6 + 2 * n_units + g]; };  // g < n_half: head units' K/V; n_half: all
   auto chk = [&](cudaError_t e) {
     if (e != cudaSuccess) ok = false;
   };
-  // Rank group g: ranks [r0, r1) own chunks [r0, r1) and [2cp - r1, 2cp - r0).
-  auto group_ranks = [&](int g, int32_t* r0, int32_t* r1) {
-    *r0 = int32_t(int64_t(g) * cp / n_groups);
-    *r1 = int32_t(int64_t(g + 1) * cp / n_groups);
-  };
-  // One contiguous range of chunks [c0, c1) of a [b, S, ...] tensor (row bytes given)
-  // or of a [b, h, S] fp32 tensor: per-batch (or per-(batch, head)) strided copies.
+  // Chunks [c0, c1) of a [b, S, ...] tensor (row bytes given): one strided copy per call.
   auto copy_tok = [&](void* dst, const void* src, int64_t c0, int64_t c1, size_t row, cudaMemcpyKind kind,
                       cudaStream_t s) {
     const size_t off = size_t(c0 * C) * row;
@@ -302,6 +321,7 @@ cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const 
                           static_cast<const uint8_t*>(src) + off, size_t(d.S) * row, size_t((c1 - c0) * C) * row,
                           size_t(d.b), kind, s));
   };
+  // Chunks [c0, c1) of a [b, h, S] fp32 tensor back to the host.
   auto copy_ml = [&](float* dst, const float* src, int64_t c0, int64_t c1, cudaStream_t s) {
     chk(cudaMemcpy2DAsync(dst + c0 * C, size_t(d.S) * 4, src + c0 * C, size_t(d.S) * 4, size_t((c1 - c0) * C) * 4,
                           size_t(d.b * d.h_q), cudaMemcpyDeviceToHost, s));
@@ -312,37 +332,53 @@ cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const 
   chk(cudaStreamWaitEvent(ps.comp[0], e_start, 0));
   chk(cudaStreamWaitEvent(ps.comp[1], e_start, 0));
   chk(cudaStreamWaitEvent(ps.out, e_start, 0));
-  chk(cudaMemcpyAsync(dk, k_host, kv_bytes, cudaMemcpyHostToDevice, ps.in));
-  chk(cudaMemcpyAsync(dv, v_host, kv_bytes, cudaMemcpyHostToDevice, ps.in));
-  chk(cudaEventRecord(e_kv, ps.in));
-  for (int g = 0; g < n_groups && ok; ++g) {
-    int32_t r0, r1;
-    group_ranks(g, &r0, &r1);
-    copy_tok(dq, q_host, r0, r1, q_row, cudaMemcpyHostToDevice, ps.in);
-    copy_tok(dq, q_host, 2 * cp - r1, 2 * cp - r0, q_row, cudaMemcpyHostToDevice, ps.in);
-    chk(cudaEventRecord(e_q(g), ps.in));
+  // Copies in: each head unit's new K/V chunks and its Q, then the remaining K/V
+  // (the tail half), then the tail units' Q.
+  int64_t kv_done = 0;
+  for (int u = 0; u < n_half && ok; ++u) {
+    int64_t c0, c1;
+    unit_chunks(u, &c0, &c1);
+    if (c1 > kv_done) {
+      copy_tok(dk, k_host, kv_done, c1, kv_row, cudaMemcpyHostToDevice, ps.in);
+      copy_tok(dv, v_host, kv_done, c1, kv_row, cudaMemcpyHostToDevice, ps.in);
+      kv_done = c1;
+    }
+    chk(cudaEventRecord(e_kv(u), ps.in));
+    copy_tok(dq, q_host, c0, c1, q_row, cudaMemcpyHostToDevice, ps.in);
+    chk(cudaEventRecord(e_q(u), ps.in));
   }
-  for (int g = 0; g < n_groups && ok; ++g) {
+  if (ok) {
+    copy_tok(dk, k_host, kv_done, 2 * cp, kv_row, cudaMemcpyHostToDevice, ps.in);
+    copy_tok(dv, v_host, kv_done, 2 * cp, kv_row, cudaMemcpyHostToDevice, ps.in);
+    chk(cudaEventRecord(e_kv(n_half), ps.in));
+  }
+  for (int u = n_half; u < n_units && ok; ++u) {
+    int64_t c0, c1;
+    unit_chunks(u, &c0, &c1);
+    copy_tok(dq, q_host, c0, c1, q_row, cudaMemcpyHostToDevice, ps.in);
+    chk(cudaEventRecord(e_q(u), ps.in));
+  }
+  // Launches (alternating compute streams) and copies out, unit by unit.
+  for (int u = 0; u < n_units && ok; ++u) {
     int32_t r0, r1;
-    group_ranks(g, &r0, &r1);
-    cudaStream_t cs = ps.comp[g & 1];
-    chk(cudaStreamWaitEvent(cs, e_kv, 0));
-    chk(cudaStreamWaitEvent(cs, e_q(g), 0));
+    int64_t c0, c1;
+    unit_ranks(u, &r0, &r1);
+    unit_chunks(u, &c0, &c1);
+    cudaStream_t cs = ps.comp[u & 1];
+    chk(cudaStreamWaitEvent(cs, e_kv(u < n_half ? u : n_half), 0));
+    chk(cudaStreamWaitEvent(cs, e_q(u), 0));
     if (!ok) break;
     st = launch_ring_attn(d, CP_LAYOUT_BALANCED, r0, r1, 0, cp, dq, dk, dv, dout, dm, dl,
-                          CP_MODE_EMIT | CP_MODE_FINALIZE, cs);
+                          CP_MODE_EMIT | CP_MODE_FINALIZE, cs, u < n_half ? kRingFirstChunk : kRingSecondChunk);
     if (st != CP_OK) {
       ok = false;
       break;
     }
-    chk(cudaEventRecord(e_c(g), cs));
-    chk(cudaStreamWaitEvent(ps.out, e_c(g), 0));
-    copy_tok(o_host, dout, r0, r1, o_row, cudaMemcpyDeviceToHost, ps.out);
-    copy_tok(o_host, dout, 2 * cp - r1, 2 * cp - r0, o_row, cudaMemcpyDeviceToHost, ps.out);
-    copy_ml(m_host, dm, r0, r1, ps.out);
-    copy_ml(m_host, dm, 2 * cp - r1, 2 * cp - r0, ps.out);
-    copy_ml(l_host, dl, r0, r1, ps.out);
-    copy_ml(l_host, dl, 2 * cp - r1, 2 * cp - r0, ps.out);
+    chk(cudaEventRecord(e_c(u), cs));
+    chk(cudaStreamWaitEvent(ps.out, e_c(u), 0));
+    copy_tok(o_host, dout, c0, c1, o_row, cudaMemcpyDeviceToHost, ps.out);
+    copy_ml(m_host, dm, c0, c1, ps.out);
+    copy_ml(l_host, dl, c0, c1, ps.out);
   }
   // Whatever was queued (also after a failure part-way), the caller's stream waits
   // for all of it, so no copy still reads or writes the caller's buffers afterwards.

@@ -105,6 +105,7 @@ struct RingParams {
   int32_t step_begin, step_end;
   int32_t mode;
   int32_t rank_begin, rank_end;  // virtual ranks whose rows this launch computes
+  int32_t chunks;                // RingChunks: both chunks of each rank, or only the first / second
   float sl;           // scale * log2(e)
 };
 
@@ -211,7 +212,7 @@ template <int LAYOUT>
 __device__ __forceinline__ Item decode_item(const RingParams& p) {
   Item it;
   const int32_t nr = p.rank_end - p.rank_begin;
-  const int32_t n_qt = 2 * nr * p.tpc;  // query tiles of the selected ranks
+  const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.tpc;  // query tiles of the selected chunks
   const int64_t per_tile = p.b * p.n_pairs;
   const int64_t idx = blockIdx.x;
   const int32_t gq = n_qt - 1 - int32_t(idx / per_tile);  // latest chunk (most keys) first
@@ -224,11 +225,14 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
   // a-th selected chunk in ascending order.  Balanced: the ranks' head chunks
   // [rank_begin, rank_end) then their tail chunks [2cp-rank_end, 2cp-rank_begin);
-  // sequential: chunks [2 rank_begin, 2 rank_end).
-  const int32_t a = gq / p.tpc;
+  // sequential: chunks [2 rank_begin, 2 rank_end).  With one chunk per rank selected,
+  // only the head (first) or only the tail (second) chunks, in ascending order.
+  int32_t a = gq / p.tpc;
   const int32_t kq = gq % p.tpc;
+  if (p.chunks == kRingSecondChunk) a += nr;
   if (LAYOUT == CP_LAYOUT_SEQUENTIAL) {
-    it.c_q = 2 * p.rank_begin + a;
+    it.c_q = (p.chunks == kRingBothChunks) ? 2 * p.rank_begin + a
+                                           : 2 * (p.rank_begin + (a % nr)) + (a >= nr ? 1 : 0);
     it.r = it.c_q / 2;
   } else {
     it.c_q = (a < nr) ? p.rank_begin + a : 2 * p.cp - p.rank_end + (a - nr);
@@ -710,7 +714,7 @@ bool ring_supported(const cp_attn_desc& d) {
 
 cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_begin, int32_t rank_end,
                            int32_t step_begin, int32_t step_end, const void* q, const void* k, const void* v,
-                           float* o, float* m, float* l, int32_t mode, cudaStream_t stream) {
+                           float* o, float* m, float* l, int32_t mode, cudaStream_t stream, int32_t chunks) {
   RingParams p;
   memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tmap_q, q, d.b, d.S, d.h_q, d.d) || !encode_map(&p.tmap_k, k, d.b, d.S, d.h_kv, d.d) ||
@@ -734,8 +738,10 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   p.mode = mode;
   p.rank_begin = rank_begin;
   p.rank_end = rank_end;
+  p.chunks = chunks;
   p.sl = d.scale * kLog2e;
-  const int64_t n_items = int64_t(2) * (rank_end - rank_begin) * p.tpc * d.b * p.n_pairs;
+  const int64_t n_items =
+      int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * p.n_pairs;
   if (n_items > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
   if (layout == CP_LAYOUT_SEQUENTIAL)
     return d.d == 128 ? launch_d<128, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream)

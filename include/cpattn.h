@@ -159,13 +159,15 @@ CPATTN_API cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t
  * copies overlap the kernels, pageable memory gives the same results more slowly.
  * `workspace` (device, caller-owned, 256-byte aligned, at least
  * cp_ring_attn_host_workspace_bytes bytes) receives the device copies of all six.
- * Pipeline: K and V are copied first (every rank's ring steps read all of them).
- * The ranks are then taken in up to 8 groups.  A group's Q rows (its ranks' two
- * chunks each) are copied in, one launch runs all cp ring steps for those rows, and
- * its O, m and l rows are copied out.  Copies in, launches (two streams, so one
+ * Pipeline, in units of chunks: the head chunks in ascending order, then the tail
+ * chunks in descending order (up to 8 units each).  Head chunk c sees only keys
+ * [0, (c+1) S/(2cp)), so K and V are copied in chunk order and a head unit waits
+ * only for the prefix it reads; the tail units wait for all of K and V.  A unit's Q
+ * rows are copied in, one launch runs all cp ring steps for those rows, and its
+ * O, m and l rows are copied out.  Copies in, launches (two streams, so one
  * launch's last CTAs overlap the next) and copies out run on separate streams
- * that the library creates once per device, so one group's copies overlap other
- * groups' computation.  The call is ordered on `cuda_stream`: it starts after the
+ * that the library creates once per device, so one unit's copies overlap other
+ * units' computation.  The call is ordered on `cuda_stream`: it starts after the
  * work queued there before it, later work queued there starts after its last
  * copy, and the workspace is in use until then.  The host is not blocked:
  * synchronise `cuda_stream` before reading the outputs.
