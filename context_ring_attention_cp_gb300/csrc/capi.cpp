@@ -438,12 +438,9 @@ cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t 
 cp_status cp_merge_tree_workspace_bytes(int64_t batch, int64_t rows, int64_t heads, int64_t d, int32_t n_parts,
                                         size_t* bytes) {
   if (bytes == nullptr || batch < 1 || rows < 1 || heads < 1 || d < 1 || n_parts < 2) return CP_ERR_INVALID_ARGUMENT;
-  if ((n_parts & (n_parts - 1)) != 0 || n_parts > (1 << 20)) return CP_ERR_INVALID_ARGUMENT;
+  if ((n_parts & (n_parts - 1)) != 0 || n_parts > CP_MAX_MERGE_PARTS) return CP_ERR_INVALID_ARGUMENT;
   if (!product_fits(n_parts, batch, rows, heads * d)) return CP_ERR_INVALID_ARGUMENT;
-  // Two ping-pong levels of at most n_parts / 2 partial triples, O then m then l, 16-byte aligned sections.
-  auto pad = [](size_t x) { return (x + 3) & ~size_t(3); };
-  const size_t half = size_t(n_parts / 2) * size_t(batch) * size_t(rows) * size_t(heads);
-  *bytes = 2 * (pad(half * size_t(d)) + 2 * pad(half)) * sizeof(float);
+  *bytes = 0;  // the tree is computed in one pass, with no intermediate levels in memory
   return CP_OK;
 }
 
@@ -451,57 +448,31 @@ cp_status cp_merge_partials_tree(int64_t batch, int64_t rows, int64_t heads, int
                                  const float* o_parts, const float* m_parts, const float* l_parts,
                                  float* workspace, size_t workspace_bytes, float* o_out, float* m_out,
                                  float* l_out, int32_t finalize, void* cuda_stream) {
+  (void)workspace;
+  (void)workspace_bytes;
   size_t need = 0;
   cp_status st = cp_merge_tree_workspace_bytes(batch, rows, heads, d, n_parts, &need);
   if (st != CP_OK) return st;
   if (d % 4 != 0) return CP_ERR_INVALID_ARGUMENT;
   if (d > 512) return CP_ERR_UNSUPPORTED;
-  if (!aligned16(o_parts) || !aligned16(m_parts) || !aligned16(l_parts) || !aligned16(workspace) ||
-      !aligned16(o_out) || !aligned16(m_out) || !aligned16(l_out))
+  if (!aligned16(o_parts) || !aligned16(m_parts) || !aligned16(l_parts) || !aligned16(o_out) ||
+      !aligned16(m_out) || !aligned16(l_out))
     return CP_ERR_INVALID_ARGUMENT;
-  if (workspace_bytes < need) return CP_ERR_INVALID_ARGUMENT;
-  auto pad = [](size_t x) { return (x + 3) & ~size_t(3); };
-  const size_t half_rows = size_t(n_parts / 2) * size_t(batch) * size_t(rows) * size_t(heads);
-  const size_t level_floats = pad(half_rows * size_t(d)) + 2 * pad(half_rows);
-  float* lvl_o[2];
-  float* lvl_m[2];
-  float* lvl_l[2];
-  for (int i = 0; i < 2; ++i) {
-    lvl_o[i] = workspace + size_t(i) * level_floats;
-    lvl_m[i] = lvl_o[i] + pad(half_rows * size_t(d));
-    lvl_l[i] = lvl_m[i] + pad(half_rows);
-  }
-  // Level k merges part i with part i + n/2 for every i < n/2: a two-part merge whose
-  // "batch" runs over (i, batch), because the part stride then is exactly n/2 parts.
-  const float* src_o = o_parts;
-  const float* src_m = m_parts;
-  const float* src_l = l_parts;
-  int cur = 0;
-  for (int64_t n = n_parts; n >= 2; n /= 2) {
-    const bool last = (n == 2);
-    MergeParams p;
-    memset(&p, 0, sizeof(p));
-    p.batch = (n / 2) * batch;
-    p.rows = rows;
-    p.heads = heads;
-    p.d = d;
-    p.n_parts = 2;
-    p.order[0] = 0;
-    p.order[1] = 1;
-    p.finalize = last && finalize != 0;
-    p.o_parts = src_o;
-    p.m_parts = src_m;
-    p.l_parts = src_l;
-    p.o_out = last ? o_out : lvl_o[cur];
-    p.m_out = last ? m_out : lvl_m[cur];
-    p.l_out = last ? l_out : lvl_l[cur];
-    if (launch_merge(p, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CP_ERR_CUDA;
-    src_o = lvl_o[cur];
-    src_m = lvl_m[cur];
-    src_l = lvl_l[cur];
-    cur ^= 1;
-  }
-  return CP_OK;
+  MergeParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = batch;
+  p.rows = rows;
+  p.heads = heads;
+  p.d = d;
+  p.n_parts = n_parts;
+  p.finalize = finalize != 0;
+  p.o_parts = o_parts;
+  p.m_parts = m_parts;
+  p.l_parts = l_parts;
+  p.o_out = o_out;
+  p.m_out = m_out;
+  p.l_out = l_out;
+  return launch_merge_tree(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 cp_status cp_passq_workspace_bytes(const cp_attn_desc* desc, size_t* bytes) {

@@ -23,6 +23,8 @@ struct MergeParams {
   uint16_t order[CP_MAX_MERGE_PARTS];  // fold order (a permutation of 0..n_parts-1)
 };
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+// The halving tree over n_parts = 2^k parts (k in 1..8) in one pass; order[] is not used.
+cudaError_t launch_merge_tree(const MergeParams& p, cudaStream_t stream);
 
 // ---- pass-Q decode partials (decode.cu) ------------------------------------
 // Key ranges per shard chosen for the device's SM count; n_parts = cp * splits.

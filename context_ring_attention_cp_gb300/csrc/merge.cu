@@ -252,7 +252,178 @@ __global__ void __launch_bounds__(kR1Threads) lse_merge_rows1_kernel(const __gri
   }
 }
 
+// Tree merge (the halving tree: at each level part i merges with part i + n/2), in
+// one pass.  That tree equals a pairwise tree over the parts taken in bit-reversed
+// index order, so each lane streams its float4 column through a stack of partial
+// results (one per level), merging whenever two of a level meet.  Every node does
+// what the two-part merge does: m = max of the children; weights e^{m_child - m}
+// (shift 0 when both are -inf); l = fmaf(w_r, l_r, w_l * l_l); O = fmaf(w_r, O_r,
+// w_l * O_l); the root is finalised like the flat merge.  The node weights of a
+// CTA's rows are computed first into shared memory, one warp per row.
+constexpr int kTreeThreads = 256;
+constexpr int kTreeWarps = kTreeThreads / 32;
+
+__device__ __forceinline__ int bit_reverse(int k, int lg) { return int(__brev(uint32_t(k)) >> (32 - lg)); }
+
+template <int LG>  // n_parts = 2^LG; the part loop below unrolls completely
+__global__ void __launch_bounds__(kTreeThreads) lse_merge_tree_kernel(const __grid_constant__ MergeParams p,
+                                                                        int rows_per_cta) {
+  extern __shared__ float smem[];
+  constexpr int lg = LG;
+  constexpr int n = 1 << LG;
+  const int nodes = n - 1;
+  float* wl = smem;                            // [rows_per_cta][nodes] left-child weights
+  float* wr = wl + rows_per_cta * nodes;       // [rows_per_cta][nodes] right-child weights
+  float* mroot = wr + rows_per_cta * nodes;    // [rows_per_cta]
+  float* lroot = mroot + rows_per_cta;         // [rows_per_cta]
+  float* scratch = lroot + rows_per_cta;       // [warps][2][n] one level's (m, l) per warp
+
+  const int64_t row_blocks = (p.rows + rows_per_cta - 1) / rows_per_cta;
+  const int64_t tile = blockIdx.x;
+  const int64_t rb = tile % row_blocks;
+  const int64_t bh = tile / row_blocks;
+  const int64_t h = bh % p.heads;
+  const int64_t bi = bh / p.heads;
+  const int64_t row0 = rb * rows_per_cta;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float* sm = scratch + warp * 2 * n;
+  float* sl = sm + n;
+
+  // Node weights, level by level; node (level L >= 1, index i) is stored at
+  // (n - (n >> (L - 1))) + i, so level 1 comes first and the root last.
+  for (int r = warp; r < rows_per_cta; r += kTreeWarps) {
+    const int64_t row = row0 + r;
+    if (row >= p.rows) break;
+    for (int k = lane; k < n; k += 32) {  // leaves in bit-reversed order
+      const int part = bit_reverse(k, lg);
+      const int64_t off = ((int64_t(part) * p.batch + bi) * p.heads + h) * p.rows + row;
+      sm[k] = p.m_parts[off];
+      sl[k] = p.l_parts[off];
+    }
+    __syncwarp();
+    int base = 0;
+    for (int L = 1; L <= lg; ++L) {
+      const int cnt = n >> L;
+      float m_new[8], l_new[8];  // up to 256 leaves: at most 128 nodes, 4 per lane
+      int c = 0;
+      for (int i = lane; i < cnt; i += 32, ++c) {
+        const float ma = sm[2 * i], mb = sm[2 * i + 1];
+        const float mx = fmaxf(ma, mb);
+        const float shift = (mx == -INFINITY) ? 0.f : mx;
+        const float wa = expf(ma - shift), wb = expf(mb - shift);
+        const float lsum = fmaf(wb, sl[2 * i + 1], fmaf(wa, sl[2 * i], 0.f));
+        wl[r * nodes + base + i] = wa;
+        wr[r * nodes + base + i] = wb;
+        m_new[c] = mx;
+        l_new[c] = lsum;
+      }
+      __syncwarp();
+      c = 0;
+      for (int i = lane; i < cnt; i += 32, ++c) {
+        sm[i] = m_new[c];
+        sl[i] = l_new[c];
+      }
+      __syncwarp();
+      base += cnt;
+    }
+    if (lane == 0) {
+      mroot[r] = sm[0];
+      lroot[r] = sl[0];
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  const int64_t n_vec = p.d / 4;
+  const int64_t part_stride = p.batch * p.rows * p.heads * p.d;
+  constexpr int kAhead = 4;  // parts of loads in flight per lane
+  for (int r = warp; r < rows_per_cta; r += kTreeWarps) {
+    const int64_t row = row0 + r;
+    if (row >= p.rows) break;
+    const int64_t obase = ((bi * p.rows + row) * p.heads + h) * p.d;
+    const float* wlr = wl + r * nodes;
+    const float* wrr = wr + r * nodes;
+    for (int64_t vi = lane; vi < n_vec; vi += 32) {
+      float4 stk[lg + 1];
+      float4 x[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead && u < n; ++u)
+        x[u] = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(bit_reverse(u, lg)) * part_stride +
+                                                         obase) + vi);
+#pragma unroll
+      for (int k = 0; k < n; ++k) {
+        float4 cur = x[k % kAhead];
+        if (k + kAhead < n)  // refill this slot with a later part
+          x[k % kAhead] = ld_stream(reinterpret_cast<const float4*>(
+                                        p.o_parts + int64_t(bit_reverse(k + kAhead, lg)) * part_stride + obase) + vi);
+        // binary counter on k: merge with the level's left partial while bit `level` of k is set
+        int base = 0;
+#pragma unroll
+        for (int level = 0; level < lg; ++level) {
+          if (((k >> level) & 1) == 0) {
+            stk[level] = cur;
+            break;
+          }
+          const int node = base + (k >> (level + 1));
+          const float a = wlr[node], b = wrr[node];
+          const float4 left = stk[level];
+          cur.x = fmaf(b, cur.x, a * left.x);
+          cur.y = fmaf(b, cur.y, a * left.y);
+          cur.z = fmaf(b, cur.z, a * left.z);
+          cur.w = fmaf(b, cur.w, a * left.w);
+          base += n >> (level + 1);
+          if (level == lg - 1) stk[lg] = cur;  // k = n - 1: the root
+        }
+      }
+      float4 y = stk[lg];
+      const float lsum = lroot[r];
+      if (p.finalize) {
+        if (lsum > 0.f) {
+          const float inv = 1.f / lsum;
+          y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
+        } else {
+          y = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      reinterpret_cast<float4*>(p.o_out + obase)[vi] = y;
+    }
+    if (lane == 0) {
+      const int64_t off = (bi * p.heads + h) * p.rows + row;
+      if (p.m_out) p.m_out[off] = mroot[r];
+      if (p.l_out) p.l_out[off] = lroot[r];
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_merge_tree(const MergeParams& p, cudaStream_t stream) {
+  int lg = 0;
+  while ((1 << lg) < p.n_parts) ++lg;
+  if ((1 << lg) != p.n_parts || lg < 1 || lg > 8) return cudaErrorInvalidValue;
+  const int rows_per_cta = p.n_parts <= 64 ? 32 : (p.n_parts <= 128 ? 16 : 8);
+  const int64_t row_blocks = (p.rows + rows_per_cta - 1) / rows_per_cta;
+  const int64_t ctas = p.batch * p.heads * row_blocks;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const size_t smem = (size_t(rows_per_cta) * (2 * (p.n_parts - 1) + 2) + size_t(kTreeWarps) * 2 * p.n_parts) *
+                      sizeof(float);
+  switch (lg) {
+#define CPATTN_TREE_CASE(L)                                                                                      \
+  case L:                                                                                                        \
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(lse_merge_tree_kernel<L>,                                       \
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=      \
+                                cudaSuccess)                                                                     \
+      return cudaErrorInvalidValue;                                                                              \
+    lse_merge_tree_kernel<L><<<unsigned(ctas), kTreeThreads, smem, stream>>>(p, rows_per_cta);                   \
+    break;
+    CPATTN_TREE_CASE(1) CPATTN_TREE_CASE(2) CPATTN_TREE_CASE(3) CPATTN_TREE_CASE(4)
+    CPATTN_TREE_CASE(5) CPATTN_TREE_CASE(6) CPATTN_TREE_CASE(7) CPATTN_TREE_CASE(8)
+#undef CPATTN_TREE_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.rows == 1) {

@@ -203,18 +203,21 @@ CPATTN_API cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t head
                             void* cuda_stream);
 
 /*
- * Tree-structured reduction of n_parts triples (n_parts a power of two >= 2), the
- * O(log cp)-depth reduce topology the spec lists as later work (Limitations
+ * Tree-structured reduction of n_parts triples (n_parts a power of two, 2..256),
+ * the O(log cp)-depth reduce topology the spec lists as later work (Limitations
  * table, "pass-Q 归约拓扑固定": Tree Attention's log-depth steps).  Level k merges
- * part i with part i + n/2 for every i, halving n, until one triple is left; each
- * level is one launch of the LSE merge kernel.  The result equals
- * cp_merge_partials up to rounding (the merge is associative).  Same layouts as
- * cp_merge_partials; `workspace` (device, caller-owned) holds two ping-pong levels
- * of n_parts/2 triples: cp_merge_tree_workspace_bytes gives its size.  Inputs are
- * not modified.
- * Errors: n_parts not a power of two >= 2, sizes < 1, d % 4 != 0, a NULL or
- * misaligned pointer, a workspace below the required size ->
- * CP_ERR_INVALID_ARGUMENT; d > 512 -> CP_ERR_UNSUPPORTED.
+ * part i with part i + n/2 for every i, halving n, until one triple is left; every
+ * node is the two-part LSE merge.  The kernel computes the whole tree in one pass
+ * over the parts (the tree is a pairwise tree over the parts in bit-reversed index
+ * order), with the same arithmetic at every node as the multi-row merge applies to
+ * two parts, so for rows > 1 the result is bit for bit what level-by-level two-part
+ * cp_merge_partials calls give (the one-row merge adds in blocks).  It equals the
+ * flat cp_merge_partials up to rounding (the merge is associative).  Same layouts
+ * as cp_merge_partials.  No workspace is needed: cp_merge_tree_workspace_bytes
+ * gives 0 and `workspace` may be NULL.  Inputs are not modified.
+ * Errors: n_parts not a power of two in 2..256, sizes < 1, d % 4 != 0, a NULL or
+ * misaligned part or output pointer -> CP_ERR_INVALID_ARGUMENT; d > 512 ->
+ * CP_ERR_UNSUPPORTED.
  */
 CPATTN_API cp_status cp_merge_tree_workspace_bytes(int64_t batch, int64_t rows, int64_t heads, int64_t d,
                                                    int32_t n_parts, size_t* bytes);

@@ -258,9 +258,13 @@ def test_tree_merge_needs_a_power_of_two(cpa, n):
     assert e.value.status == 1
 
 
-def test_tree_merge_workspace_size(cpa):
-    # two ping-pong levels of n/2 triples: O (d floats) + m + l per (part, batch, row, head)
-    assert cpa.cp_merge_tree_workspace_bytes(1, 4096, 64, 128, 32) == 2 * 16 * 4096 * 64 * (128 + 2) * 4
+def test_tree_merge_needs_no_workspace_and_at_most_256_parts(cpa):
+    # the tree is computed in one pass: no intermediate levels in memory
+    assert cpa.cp_merge_tree_workspace_bytes(1, 4096, 64, 128, 32) == 0
+    assert cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, 256) == 0
+    with pytest.raises(cpa.CpError) as e:
+        cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, 512)
+    assert e.value.status == 1
 
 
 def _round256(x):

@@ -171,9 +171,34 @@ def test_tree_merge_rejects_bad_part_counts():
     ml = torch.empty((1, 2, 8), dtype=torch.float32, device="cuda")
     with pytest.raises(cpa.CpError):
         cpa.cp_merge_partials_tree(1, 8, 2, 8, 3, o, m, l, ws, ws.numel() * 4, out, ml, ml.clone())
-    need = cpa.cp_merge_tree_workspace_bytes(1, 8, 2, 8, 2)
-    with pytest.raises(cpa.CpError):
-        cpa.cp_merge_partials_tree(1, 8, 2, 8, 2, o[:2], m[:2], l[:2], ws, need - 4, out, ml, ml.clone())
+
+
+@pytest.mark.parametrize("shape", [(2, 2, 33, 3, 64), (8, 2, 33, 3, 64), (32, 1, 64, 4, 128), (256, 1, 16, 2, 16)])
+def test_tree_merge_equals_level_by_level_two_part_merges(shape):
+    # The one-pass tree does at every node what a two-part merge does, so it must
+    # equal the halving tree run level by level through cp_merge_partials bit for bit.
+    n, b, rows, heads, d = shape
+    draws = [synth.merge_parts(n, heads, rows, d, spread=80.0, seed=11 * n + bi) for bi in range(b)]
+    o = torch.cat([x[0] for x in draws], dim=1).contiguous()
+    m = torch.cat([x[1] for x in draws], dim=1).contiguous()
+    l = torch.cat([x[2] for x in draws], dim=1).contiguous()
+    for fin in (False, True):
+        to, tm, tl = _merge_tree(o, m, l, finalize=fin)
+        lo, lm, ll = o, m, l
+        k = n
+        while k >= 2:
+            # level: part i with part i + k/2, as one two-part merge over (i, batch)
+            last = k == 2
+            oo = torch.empty((k // 2 * b, rows, heads, d), dtype=torch.float32, device="cuda")
+            mo = torch.empty((k // 2 * b, heads, rows), dtype=torch.float32, device="cuda")
+            lo2 = torch.empty_like(mo)
+            cpa.cp_merge_partials(k // 2 * b, rows, heads, d, 2, lo, lm, ll, oo, mo, lo2, finalize=fin and last)
+            lo = oo.view(k // 2, b, rows, heads, d)
+            lm = mo.view(k // 2, b, heads, rows)
+            ll = lo2.view(k // 2, b, heads, rows)
+            k //= 2
+        torch.cuda.synchronize()
+        assert torch.equal(tm, lm[0]) and torch.equal(tl, ll[0]) and torch.equal(to, lo[0]), f"{shape} fin={fin}"
 
 
 # ------------------------------------------------------------------ decode
