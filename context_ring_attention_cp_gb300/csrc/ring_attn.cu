@@ -546,6 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const float inv = (fin && l_out > 0.f) ? 1.f / l_out : (fin ? 0.f : 1.f);
       const float wnew = beta * fre * inv;
       const float wold = alpha * inv;
+      // Without ACCUMULATE the two factors are applied in turn, (O * 2^(m_ref - m_true)) / l,
+      // exactly as an EMIT launch followed by a one-part finalising merge does, so the
+      // fused result is bit for bit the same as that pair.
+      const float wre = beta * fre;
+      auto plain = [&](uint32_t bits) { return (__uint_as_float(bits) * wre) * inv; };
       // A whole 128-row tile written plainly goes through shared memory and TMA tile
       // stores (128 rows x 32 floats a box); partial tiles and ACCUMULATE store
       // each row directly.  Staging: tile A uses the Q tiles' space, tile B two K/V
@@ -567,9 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           const uint32_t rowa = stage + uint32_t(c * BM * 128 + t * 128);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            st_shared_v4(rowa + uint32_t(((k ^ (t & 7)) << 4)), __uint_as_float(r[4 * k]) * wnew,
-                         __uint_as_float(r[4 * k + 1]) * wnew, __uint_as_float(r[4 * k + 2]) * wnew,
-                         __uint_as_float(r[4 * k + 3]) * wnew);
+            st_shared_v4(rowa + uint32_t(((k ^ (t & 7)) << 4)), plain(r[4 * k]), plain(r[4 * k + 1]),
+                         plain(r[4 * k + 2]), plain(r[4 * k + 3]));
         }
         fence_async_smem();
         __syncwarp();
@@ -599,16 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 v;
-              v.x = __uint_as_float(r[i]) * wnew;
-              v.y = __uint_as_float(r[i + 1]) * wnew;
-              v.z = __uint_as_float(r[i + 2]) * wnew;
-              v.w = __uint_as_float(r[i + 3]) * wnew;
               if (p.mode & CP_MODE_ACCUMULATE) {
                 const float4 old = *reinterpret_cast<const float4*>(orow + c * 32 + i);
-                v.x = fmaf(old.x, wold, v.x);
-                v.y = fmaf(old.y, wold, v.y);
-                v.z = fmaf(old.z, wold, v.z);
-                v.w = fmaf(old.w, wold, v.w);
+                v.x = fmaf(old.x, wold, __uint_as_float(r[i]) * wnew);
+                v.y = fmaf(old.y, wold, __uint_as_float(r[i + 1]) * wnew);
+                v.z = fmaf(old.z, wold, __uint_as_float(r[i + 2]) * wnew);
+                v.w = fmaf(old.w, wold, __uint_as_float(r[i + 3]) * wnew);
+              } else {
+                v = make_float4(plain(r[i]), plain(r[i + 1]), plain(r[i + 2]), plain(r[i + 3]));
               }
               *reinterpret_cast<float4*>(orow + c * 32 + i) = v;
             }

@@ -123,6 +123,20 @@ def test_two_step_ranges_accumulate_to_full():
     assert_out_close(bufs[0].cpu().numpy(), ref_out, "two ranges")
 
 
+@pytest.mark.parametrize("case", [(1, 1536, 4, 2, 128, 1), (2, 1000, 3, 3, 64, 1), (1, 2048, 8, 2, 128, 4)])
+def test_fused_finalize_is_bit_identical_to_emit_then_one_part_merge(case):
+    # cp = 1 degeneracy (and any cp): the fused EMIT | FINALIZE launch equals an EMIT
+    # launch followed by the merge kernel finalising its single part, bit for bit.
+    b, S, hq, hkv, d, cp = case
+    q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=sum(case))
+    fo, fm, fl = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    eo, em, el = run_ring(q, k, v, cp, 0, cp, EMIT)
+    out = torch.empty_like(eo); mo = torch.empty_like(em); lo = torch.empty_like(el)
+    cpa.cp_merge_partials(b, S, hq, d, 1, eo, em, el, out, mo, lo, finalize=True)
+    torch.cuda.synchronize()
+    assert torch.equal(mo, fm) and torch.equal(lo, fl) and torch.equal(out, fo)
+
+
 def test_cp1_equals_unsplit_and_any_cp_agrees():
     b, S, hq, hkv, d = 1, 1536, 4, 2, 128
     q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=8)
