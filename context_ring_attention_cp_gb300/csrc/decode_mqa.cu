@@ -15,15 +15,18 @@
 //                   (A = V tile read MN-major, B = P^T written by the softmax warps)
 // so g = 16 heads fill an N = 16 instruction with no padding.  K and V stream
 // through a ring of 16 KB slots (128 keys x 64 d, 128-byte swizzle), loaded in
-// exactly the order the MMAs consume them: K_0, then (K_{j+1}, V_j) per tile.
+// exactly the order the MMAs consume them: K_0, then (K_{j+1}, V_j) per tile; V_j
+// is requested only once P(j) is written, so its slots hold loads in flight, not
+// landed data waiting for softmax(j).
 // A tile's V slabs come in groups of d/64 >= 2 starting on an even slot of an
 // even-sized ring, so the two 64-wide halves of a d block sit in adjacent slots
 // and the MN-major descriptor's leading offset is one slot.
 //
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer (one lane), 4-7 softmax and
 // epilogue (thread = key lane of S^T, and = d lane of O^T).  Per-head maxima over
-// the 128 keys of a tile come from a warp butterfly plus a shared-memory reduction
-// across the four warps; the exponent reference is raised only when a head's max
+// the 128 keys of a tile come from a warp max reduction (redux.sync) plus a
+// shared-memory reduction across the four warps; the exponent reference is raised
+// only when a head's max
 // grows by more than 8 (log2 units), O^T columns are then rescaled in TMEM.  Row
 // sums stay per thread until the epilogue.  The CTA writes its partial triple per
 // query head to the decode workspace, which the LSE merge kernel reduces.
@@ -168,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int32_t li = 0;  // running slab index, in MMA consumption order
+      int32_t jt = 0;  // running tile index (P barrier phases)
       bool ok = true;
       int32_t ic = 0;  // items of this CTA so far
       for (int32_t item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++ic) {
@@ -193,8 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1) mqa_decode_kernel(const __grid_co
         load_tile(&p.tmap_k, 0);
         for (int32_t j = 0; ok && j < n_tiles; ++j) {
           if (j + 1 < n_tiles) load_tile(&p.tmap_k, j + 1);
+          // V_j is consumed only once P(j) is written: loading it then keeps its slots
+          // free for loads in flight while softmax(j) runs.
+          const int32_t t = jt + j;
+          if (ok && !wait(bar_p(t & 1), uint32_t((t >> 1) & 1))) { ok = false; break; }
           if (ok) load_tile(&p.tmap_v, j);
         }
+        jt += n_tiles;
       }
       if (!ok) {
         const uint64_t t0 = globaltimer();
