@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kTreeThreads) lse_merge_tree_kernel(const __gr
 
   const int64_t n_vec = p.d / 4;
   const int64_t part_stride = p.batch * p.rows * p.heads * p.d;
-  constexpr int kAhead = 4;  // parts of loads in flight per lane
+  constexpr int kAhead = 8;  // parts of loads in flight per lane
   for (int r = warp; r < rows_per_cta; r += kTreeWarps) {
     const int64_t row = row0 + r;
     if (row >= p.rows) break;
