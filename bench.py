@@ -582,6 +582,15 @@ def profile_case(name, steps):
         fn = lambda: cpa.cp_merge_partials(1, w["rows"], w["heads"], w["d"], w["parts"], po, pm, pl, mo, mm, ml,  # noqa
                                            stream=stream)
         work = merge_bytes(w)
+    elif name == "merge-tree":  # the merge-stress parts reduced as the halving tree, one pass
+        w = synth.WORKLOADS["merge"]
+        po, pm, pl = synth.merge_parts(w["parts"], w["heads"], w["rows"], w["d"], spread=w["spread"], seed=w["seed"])
+        mo = torch.empty((1, w["rows"], w["heads"], w["d"]), dtype=torch.float32, device="cuda")
+        mm = torch.empty((1, w["heads"], w["rows"]), dtype=torch.float32, device="cuda")
+        ml = torch.empty_like(mm)
+        fn = lambda: cpa.cp_merge_partials_tree(1, w["rows"], w["heads"], w["d"], w["parts"], po, pm, pl, None, 0,  # noqa
+                                                mo, mm, ml, stream=stream)
+        work = merge_bytes(w)
     else:
         raise SystemExit(f"unknown --case {name}")
     for _ in range(3):
@@ -601,7 +610,7 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--case", choices=["decode-small", "decode-shared-kv", "merge"], default=None,
+    ap.add_argument("--case", choices=["decode-small", "decode-shared-kv", "merge", "merge-tree"], default=None,
                     help="time one kernel on a capture-sized case (for ncu) instead of the benchmark")
     args = ap.parse_args()
     if args.case is not None:
