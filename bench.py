@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "94ac04302df5ca13", "bytes": 2322920704}
+RING_TRAFFIC = {"sha256_prefix": "c7a15816d027ac1e", "bytes": 2325217024}
 
 
 def ring_traffic():
