@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "c7a15816d027ac1e", "bytes": 2325217024}
+RING_TRAFFIC = {"sha256_prefix": "2e9b09ec2bb819a7", "bytes": 2315439104}
 
 
 def ring_traffic():
@@ -400,6 +400,19 @@ def secondary_lines(cpa, synth, peaks, stream):
     tf = step_flops / (ms * 1e-3) / 1e12
     out["prefill_one_step_emit"] = {
         "workload": "one ring step (t=1, all 8 virtual ranks, EMIT) of the GQA prefill workload",
+        "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
+        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+    # the same step merged into a running triple (what every step after the first does
+    # when each rank launches per step): O, m and l are read as well as written
+    cpa.cp_ring_step_partial_attn(desc, 0, 1, q, k, v, o, m, l, cpa.CP_MODE_EMIT, stream)
+    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, cpa.CP_MODE_ACCUMULATE, stream)  # noqa
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 20, stream)
+    tf = step_flops / (ms * 1e-3) / 1e12
+    out["prefill_one_step_accumulate"] = {
+        "workload": "one ring step (t=1, all 8 virtual ranks, ACCUMULATE into the step-0 triple) "
+                    "of the GQA prefill workload",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
         "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l

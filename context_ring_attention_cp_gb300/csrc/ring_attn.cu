@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   auto bar_p = [&](int tt) { return smem_u32(&bars[3 + 2 * K::kStages + tt]); };
   auto bar_o = [&](int tt) { return smem_u32(&bars[5 + 2 * K::kStages + tt]); };
   auto bar_e = [&](int tt) { return smem_u32(&bars[7 + 2 * K::kStages + tt]); };  // O tile staged
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[10 + 2 * K::kStages]);
+  auto bar_l = [&](int tt) { return smem_u32(&bars[9 + 2 * K::kStages + tt]); };  // old O tile loaded
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[11 + 2 * K::kStages]);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       mbar_init(bar_p(tt), BM / 32);
       mbar_init(bar_o(tt), 1);
       mbar_init(bar_e(tt), BM / 32);
+      mbar_init(bar_l(tt), 1);
     }
     // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) ? 1 : 0;
@@ -322,8 +324,27 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       bool diag;
       int32_t li = 0;  // load index: K_j = 2j, V_j = 2j + 1
       bool ok = true;
+      // ACCUMULATE reads the running triple at the end: bring its O tiles and m, l rows
+      // into L2 once the K/V pipeline is full, so that they do not delay the first loads.
+      const bool staged = it.q_rows == BM && it.q_row0 + BM <= p.S;
+      bool prefetched = (p.mode & CP_MODE_ACCUMULATE) == 0;
+      auto prefetch_old = [&]() {
+        for (int tt = 0; tt < n_q; ++tt) {
+          const int64_t ml = (int64_t(it.bi) * p.h_q + it.h0 + tt) * p.S + it.q_row0;
+          for (int i = 0; i < it.q_rows; i += 32) {
+            prefetch_l2(p.m + ml + i);
+            prefetch_l2(p.l + ml + i);
+          }
+          prefetch_l2(p.m + ml + it.q_rows - 1);
+          prefetch_l2(p.l + ml + it.q_rows - 1);
+          if (staged)
+            for (int c = 0; c < D / 32; ++c) tma_prefetch_4d(&p.tmap_o, c * 32, it.h0 + tt, it.q_row0, it.bi);
+        }
+        prefetched = true;
+      };
       while (ok && cur.next(key0, key_end, diag)) {
         for (int which = 0; which < 2 && ok; ++which, ++li) {
+          if (!prefetched && li == K::kStages) prefetch_old();
           const int s = li % K::kStages;
           const int round = li / K::kStages;
           if (round > 0 && !mbar_wait(bar_empty(s), uint32_t((round - 1) & 1), abort_flag)) {
@@ -337,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
                         key0, it.bi);
         }
       }
+      if (ok && !prefetched) prefetch_old();
       if (!ok) {  // let copies in flight land before the CTA can exit
         const uint64_t t0 = globaltimer();
         while (globaltimer() - t0 < 50000ull) {
@@ -531,9 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const float m_new_nat = m_true * kLn2;
       const float l_new = l_run * fre;
       const bool row_ok = t < it.q_rows && row < p.S;
+      const bool accumulate = (p.mode & CP_MODE_ACCUMULATE) != 0;
+      // A whole 128-row tile moves its O rows through shared memory with TMA.
+      const bool staged = it.q_rows == BM && it.q_row0 + BM <= p.S;
       const int64_t ml_off = (int64_t(it.bi) * p.h_q + h) * p.S + row;
       float alpha = 0.f, beta = 1.f, l_out = l_new, m_out = m_new_nat;
-      if ((p.mode & CP_MODE_ACCUMULATE) && row_ok) {
+      if (accumulate && row_ok) {
         const float m_old = p.m[ml_off];
         const float l_old = p.l[ml_off];
         m_out = fmaxf(m_old, m_new_nat);
@@ -551,13 +576,30 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       // fused result is bit for bit the same as that pair.
       const float wre = beta * fre;
       auto plain = [&](uint32_t bits) { return (__uint_as_float(bits) * wre) * inv; };
-      // A whole 128-row tile written plainly goes through shared memory and TMA tile
-      // stores (128 rows x 32 floats a box); partial tiles and ACCUMULATE store
-      // each row directly.  Staging: tile A uses the Q tiles' space, tile B two K/V
-      // slots; every MMA that read them has completed once bar_o(tt) has fired.
-      const bool staged = !(p.mode & CP_MODE_ACCUMULATE) && it.q_rows == BM && it.q_row0 + BM <= p.S;
-      if (staged) {
-        const uint32_t stage = sbase + (tt == 0 ? uint32_t(K::kQOff) : uint32_t(K::kKvOff));
+      // A whole 128-row tile goes through shared memory: ACCUMULATE first loads the
+      // old O tile there, each thread combines its row in place, and TMA tile stores
+      // (128 rows x 32 floats a box) write it out.  Partial tiles read and store each
+      // row directly.  Staging: tile A uses the Q tiles' space, tile B two K/V slots;
+      // every MMA that read them has completed once bar_o(tt) has fired.
+      const uint32_t stage = sbase + (tt == 0 ? uint32_t(K::kQOff) : uint32_t(K::kKvOff));
+      if (staged && accumulate) {
+        const bool leader = warp == 4 + 4 * tt && lane == 0;
+        if (leader) {
+          mbar_expect_tx(bar_l(tt), uint32_t(BM * D * 4));
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tma_load_4d(stage + uint32_t(c * BM * 128), &p.tmap_o, bar_l(tt), c * 32, h, it.q_row0, it.bi);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_l(tt), 0, abort_flag))) {
+          ok = false;
+          if (leader) {  // let the copies in flight land before the CTA can exit
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 50000ull) {
+            }
+          }
+        }
+      }
+      if (staged && ok) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -571,9 +613,18 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           // box c, row t, 16-byte chunk k at position k ^ (t % 8) (128-byte swizzle)
           const uint32_t rowa = stage + uint32_t(c * BM * 128 + t * 128);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            st_shared_v4(rowa + uint32_t(((k ^ (t & 7)) << 4)), plain(r[4 * k]), plain(r[4 * k + 1]),
-                         plain(r[4 * k + 2]), plain(r[4 * k + 3]));
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t a = rowa + uint32_t(((k ^ (t & 7)) << 4));
+            if (accumulate) {
+              const float4 old = ld_shared_v4(a);
+              st_shared_v4(a, fmaf(old.x, wold, __uint_as_float(r[4 * k]) * wnew),
+                           fmaf(old.y, wold, __uint_as_float(r[4 * k + 1]) * wnew),
+                           fmaf(old.z, wold, __uint_as_float(r[4 * k + 2]) * wnew),
+                           fmaf(old.w, wold, __uint_as_float(r[4 * k + 3]) * wnew));
+            } else {
+              st_shared_v4(a, plain(r[4 * k]), plain(r[4 * k + 1]), plain(r[4 * k + 2]), plain(r[4 * k + 3]));
+            }
+          }
         }
         fence_async_smem();
         __syncwarp();
@@ -587,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
             bulk_wait_all();
           }
         }
-      } else {
+      } else if (ok) {
         float* orow = p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + h) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -603,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 v;
-              if (p.mode & CP_MODE_ACCUMULATE) {
+              if (accumulate) {
                 const float4 old = *reinterpret_cast<const float4*>(orow + c * 32 + i);
                 v.x = fmaf(old.x, wold, __uint_as_float(r[i]) * wnew);
                 v.y = fmaf(old.y, wold, __uint_as_float(r[i + 1]) * wnew);
@@ -617,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && ok) {
         p.m[ml_off] = m_out;
         p.l[ml_off] = l_out;
       }

@@ -82,7 +82,8 @@ def test_each_step_emits_the_oracle_step_triple(case):
             assert_out_close(go[live] / gl[live][:, None], ref_out, f"step {t} rank {r}")
 
 
-@pytest.mark.parametrize("case", [SMALL[1], SMALL[3], SMALL[7]], ids=["b2", "ragged_g3", "cp5"])
+@pytest.mark.parametrize("case", [SMALL[1], SMALL[3], SMALL[7], (1, 2048, 8, 2, 128, 4, 0.5)],
+                         ids=["b2", "ragged_g3", "cp5", "whole_tiles_gqa4"])
 def test_accumulate_steps_then_finalize(case):
     b, S, hq, hkv, d, cp, std = case
     q, k, v = _inputs(b, S, hq, hkv, d, std, seed=99)
@@ -94,6 +95,22 @@ def test_accumulate_steps_then_finalize(case):
     ref_out, ref_m, ref_l, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
     assert_out_close(bufs[0].cpu().numpy(), ref_out, "accumulated")
     assert np.abs(bufs[1].cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("case", [SMALL[1], SMALL[2], SMALL[3], SMALL[4]],
+                         ids=["b2", "ragged_250", "ragged_g3", "c128"])
+def test_accumulate_into_the_identity_triple_equals_emit(case):
+    # Against m = -inf, l = 0, O = 0 the merge weights are alpha = 0 and beta = 1, so
+    # ACCUMULATE stores fmaf(0, 0, O * f) = O * f: the value EMIT stores, bit for bit.
+    # Whole 128-row tiles combine in shared memory, ragged ones row by row; both are held
+    # to EMIT here, at every step.
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=31)
+    for t in range(cp):
+        acc = run_ring(q, k, v, cp, t, t + 1, ACC, ring_buffers(b, S, hq, d, identity=True))
+        emit = run_ring(q, k, v, cp, t, t + 1, EMIT)
+        for x, y in zip(acc, emit):
+            assert torch.equal(x, y), f"step {t}"
 
 
 def test_emit_then_merge_kernel_finalize_matches_fused():
