@@ -262,11 +262,13 @@ __global__ void __launch_bounds__(kR1Threads) lse_merge_rows1_kernel(const __gri
 // CTA's rows are computed first into shared memory, one warp per row.
 constexpr int kTreeThreads = 256;
 constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kTreeGroupLg = 5;  // trees above 32 leaves run as a loop over 32-leaf subtrees
+constexpr int kRing = 8;         // parts of loads in flight per lane in that loop
 
 __device__ __forceinline__ int bit_reverse(int k, int lg) { return int(__brev(uint32_t(k)) >> (32 - lg)); }
 
 template <int LG>  // n_parts = 2^LG; the part loop below unrolls completely
-__global__ void __launch_bounds__(kTreeThreads) lse_merge_tree_kernel(const __grid_constant__ MergeParams p,
+__global__ void __launch_bounds__(kTreeThreads, 3) lse_merge_tree_kernel(const __grid_constant__ MergeParams p,
                                                                         int rows_per_cta) {
   extern __shared__ float smem[];
   constexpr int lg = LG;
@@ -336,7 +338,7 @@ __global__ void __launch_bounds__(kTreeThreads) lse_merge_tree_kernel(const __gr
 
   const int64_t n_vec = p.d / 4;
   const int64_t part_stride = p.batch * p.rows * p.heads * p.d;
-  constexpr int kAhead = 8;  // parts of loads in flight per lane
+  constexpr int kAhead = 14;  // parts of loads in flight per lane
   for (int r = warp; r < rows_per_cta; r += kTreeWarps) {
     const int64_t row = row0 + r;
     if (row >= p.rows) break;
@@ -344,38 +346,92 @@ __global__ void __launch_bounds__(kTreeThreads) lse_merge_tree_kernel(const __gr
     const float* wlr = wl + r * nodes;
     const float* wrr = wr + r * nodes;
     for (int64_t vi = lane; vi < n_vec; vi += 32) {
-      float4 stk[lg + 1];
-      float4 x[kAhead];
+      float4 y;
+      // One tree node: cur = w_r * cur + w_l * left, weights from shared memory.
+      auto node_merge = [&](float4& cur, const float4& left, int node) {
+        const float a = wlr[node], b = wrr[node];
+        cur.x = fmaf(b, cur.x, a * left.x);
+        cur.y = fmaf(b, cur.y, a * left.y);
+        cur.z = fmaf(b, cur.z, a * left.z);
+        cur.w = fmaf(b, cur.w, a * left.w);
+      };
+      if constexpr (LG <= kTreeGroupLg) {
+        // All n leaves unrolled: a stack of one partial per level.
+        float4 stk[lg + 1];
+        float4 x[kAhead];
 #pragma unroll
-      for (int u = 0; u < kAhead && u < n; ++u)
-        x[u] = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(bit_reverse(u, lg)) * part_stride +
-                                                         obase) + vi);
+        for (int u = 0; u < kAhead && u < n; ++u)
+          x[u] = ld_stream(reinterpret_cast<const float4*>(p.o_parts + int64_t(bit_reverse(u, lg)) * part_stride +
+                                                           obase) + vi);
 #pragma unroll
-      for (int k = 0; k < n; ++k) {
-        float4 cur = x[k % kAhead];
-        if (k + kAhead < n)  // refill this slot with a later part
-          x[k % kAhead] = ld_stream(reinterpret_cast<const float4*>(
-                                        p.o_parts + int64_t(bit_reverse(k + kAhead, lg)) * part_stride + obase) + vi);
-        // binary counter on k: merge with the level's left partial while bit `level` of k is set
-        int base = 0;
+        for (int k = 0; k < n; ++k) {
+          float4 cur = x[k % kAhead];
+          if (k + kAhead < n)  // refill this slot with a later part
+            x[k % kAhead] = ld_stream(reinterpret_cast<const float4*>(
+                                          p.o_parts + int64_t(bit_reverse(k + kAhead, lg)) * part_stride + obase) + vi);
+          // binary counter on k: merge with the level's left partial while bit `level` of k is set
+          int base = 0;
 #pragma unroll
-        for (int level = 0; level < lg; ++level) {
-          if (((k >> level) & 1) == 0) {
-            stk[level] = cur;
-            break;
+          for (int level = 0; level < lg; ++level) {
+            if (((k >> level) & 1) == 0) {
+              stk[level] = cur;
+              break;
+            }
+            node_merge(cur, stk[level], base + (k >> (level + 1)));
+            base += n >> (level + 1);
+            if (level == lg - 1) stk[lg] = cur;  // k = n - 1: the root
           }
-          const int node = base + (k >> (level + 1));
-          const float a = wlr[node], b = wrr[node];
-          const float4 left = stk[level];
-          cur.x = fmaf(b, cur.x, a * left.x);
-          cur.y = fmaf(b, cur.y, a * left.y);
-          cur.z = fmaf(b, cur.z, a * left.z);
-          cur.w = fmaf(b, cur.w, a * left.w);
-          base += n >> (level + 1);
-          if (level == lg - 1) stk[lg] = cur;  // k = n - 1: the root
+        }
+        y = stk[lg];
+      } else {
+        // Leaves in groups of 2^kTreeGroupLg: each group's subtree is unrolled as above,
+        // the groups run in a loop, and the levels above a group keep their own stack.
+        // The same nodes in the same order as the single unrolled tree.
+        constexpr int G = kTreeGroupLg;
+        constexpr int ng = 1 << G;
+        constexpr int UP = LG - G;
+        const float* col = p.o_parts + obase + 4 * vi;
+        auto leaf = [&](int k) {
+          return ld_stream(reinterpret_cast<const float4*>(col + int64_t(bit_reverse(k, lg)) * part_stride));
+        };
+        float4 up[UP];
+        float4 x[kRing];  // kRing divides ng, so a leaf's slot is the same in every group
+#pragma unroll
+        for (int u = 0; u < kRing; ++u) x[u] = leaf(u);
+#pragma unroll 1
+        for (int g = 0; g < (1 << UP); ++g) {
+          float4 stk[G];
+          float4 cur;
+#pragma unroll
+          for (int k = 0; k < ng; ++k) {
+            cur = x[k % kRing];
+            const int next = g * ng + k + kRing;
+            if (next < n) x[k % kRing] = leaf(next);
+            int base = 0;
+#pragma unroll
+            for (int level = 0; level < G; ++level) {
+              if (((k >> level) & 1) == 0) {
+                stk[level] = cur;
+                break;
+              }
+              node_merge(cur, stk[level], base + g * (ng >> (level + 1)) + (k >> (level + 1)));
+              base += n >> (level + 1);
+            }
+          }
+          // cur is group g's subtree root: carry it up the binary counter on g
+          int base = n - (n >> G);
+#pragma unroll
+          for (int lv = 0; lv < UP; ++lv) {
+            if (((g >> lv) & 1) == 0) {
+              up[lv] = cur;
+              break;
+            }
+            node_merge(cur, up[lv], base + (g >> (lv + 1)));
+            base += n >> (G + lv + 1);
+          }
+          y = cur;  // the root after the last group
         }
       }
-      float4 y = stk[lg];
       const float lsum = lroot[r];
       if (p.finalize) {
         if (lsum > 0.f) {

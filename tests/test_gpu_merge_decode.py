@@ -173,7 +173,8 @@ def test_tree_merge_rejects_bad_part_counts():
         cpa.cp_merge_partials_tree(1, 8, 2, 8, 3, o, m, l, ws, ws.numel() * 4, out, ml, ml.clone())
 
 
-@pytest.mark.parametrize("shape", [(2, 2, 33, 3, 64), (8, 2, 33, 3, 64), (32, 1, 64, 4, 128), (256, 1, 16, 2, 16)])
+@pytest.mark.parametrize("shape", [(2, 2, 33, 3, 64), (8, 2, 33, 3, 64), (32, 1, 64, 4, 128), (64, 2, 20, 3, 32),
+                                   (128, 1, 24, 2, 64), (256, 1, 16, 2, 16)])
 def test_tree_merge_equals_level_by_level_two_part_merges(shape):
     # The one-pass tree does at every node what a two-part merge does, so it must
     # equal the halving tree run level by level through cp_merge_partials bit for bit.
