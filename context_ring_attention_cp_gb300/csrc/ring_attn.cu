@@ -313,11 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && n_kv > 0) {
+      // L2 policy: a Q tile is read by this CTA alone, while every query tile of the
+      // kv head re-reads its K/V tiles, so K/V should outlive Q (and O) in L2.
+      const uint64_t pol_once = l2_policy_evict_first();
       mbar_expect_tx(bar_q, uint32_t(n_q * K::kTileBytes));
       for (int tt = 0; tt < n_q; ++tt)
         for (int sl = 0; sl < K::kSlabs; ++sl)
-          tma_load_4d(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
-                      it.h0 + tt, it.q_row0, it.bi);
+          tma_load_4d_hint(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
+                           it.h0 + tt, it.q_row0, it.bi, pol_once);
       KvCursor<LAYOUT> cur;
       cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
       int32_t key0, key_end;
@@ -354,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           mbar_expect_tx(bar_full(s), uint32_t(K::kTileBytes));
           const CUtensorMap* map = which == 0 ? &p.tmap_k : &p.tmap_v;
           for (int sl = 0; sl < K::kSlabs; ++sl)
-            tma_load_4d(sbase + K::kKvOff + s * K::kTileBytes + sl * K::kSlab, map, bar_full(s), sl * 64, it.kvh,
-                        key0, it.bi);
+            tma_load_4d_hint(sbase + K::kKvOff + s * K::kTileBytes + sl * K::kSlab, map, bar_full(s), sl * 64,
+                             it.kvh, key0, it.bi, l2_policy_evict_last());
         }
       }
       if (ok && !prefetched) prefetch_old();
@@ -631,9 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         if (lane == 0) mbar_arrive(bar_e(tt));
         if (warp == 4 + 4 * tt && lane == 0) {
           if (mbar_wait(bar_e(tt), 0, abort_flag)) {
+            const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c)
-              tma_store_4d(&p.tmap_o, stage + uint32_t(c * BM * 128), c * 32, h, it.q_row0, it.bi);
+              tma_store_4d_hint(&p.tmap_o, stage + uint32_t(c * BM * 128), c * 32, h, it.q_row0, it.bi, pol_once);
             bulk_commit();
             bulk_wait_all();
           }
