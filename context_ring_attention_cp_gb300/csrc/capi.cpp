@@ -108,13 +108,53 @@ bool pipe_streams(PipeStreams* out) {
   if (!made[dev]) {
     PipeStreams s;
     cudaStream_t* all[4] = {&s.in, &s.comp[0], &s.comp[1], &s.out};
-    for (cudaStream_t* x : all)
-      if (cudaStreamCreateWithFlags(x, cudaStreamNonBlocking) != cudaSuccess) return false;
+    for (int i = 0; i < 4; ++i) {
+      if (cudaStreamCreateWithFlags(all[i], cudaStreamNonBlocking) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaStreamDestroy(*all[j]);
+        return false;
+      }
+    }
     per_dev[dev] = s;
     made[dev] = true;
   }
   *out = per_dev[dev];
   return true;
+}
+
+// Merge of n_parts triples in index order (the caller may set another order).
+MergeParams merge_params(int64_t batch, int64_t rows, int64_t heads, int64_t d, int32_t n_parts,
+                         const float* o_parts, const float* m_parts, const float* l_parts, float* o_out,
+                         float* m_out, float* l_out, bool finalize) {
+  MergeParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = batch;
+  p.rows = rows;
+  p.heads = heads;
+  p.d = d;
+  p.n_parts = n_parts;
+  p.finalize = finalize;
+  p.o_parts = o_parts;
+  p.m_parts = m_parts;
+  p.l_parts = l_parts;
+  p.o_out = o_out;
+  p.m_out = m_out;
+  p.l_out = l_out;
+  for (int32_t i = 0; i < n_parts; ++i) p.order[i] = static_cast<uint16_t>(i);
+  return p;
+}
+
+// Pass-Q decode after the checks: the shard partials into the given sections, then the
+// three-quantity reduce (the LSE merge over the parts in shard order, finalised).
+cp_status run_passq_decode(const cp_attn_desc& desc, int32_t splits, const void* q, const void* k, const void* v,
+                           float* sections, float* out, float* m_out, float* l_out, cudaStream_t s) {
+  const int64_t n_parts = desc.cp * splits;
+  if (n_parts > CP_MAX_MERGE_PARTS) return CP_ERR_UNSUPPORTED;
+  float *o_parts = nullptr, *m_parts = nullptr, *l_parts = nullptr;
+  decode_workspace_sections(desc, splits, sections, &o_parts, &m_parts, &l_parts);
+  if (launch_decode_partials(desc, splits, q, k, v, o_parts, m_parts, l_parts, s) != cudaSuccess) return CP_ERR_CUDA;
+  const MergeParams p =
+      merge_params(desc.b, 1, desc.h_q, desc.d, int32_t(n_parts), o_parts, m_parts, l_parts, out, m_out, l_out, true);
+  return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
 }  // namespace
@@ -407,8 +447,8 @@ cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t 
   if (!aligned16(o_parts) || !aligned16(m_parts) || !aligned16(l_parts) || !aligned16(o_out) ||
       !aligned16(m_out) || !aligned16(l_out))
     return CP_ERR_INVALID_ARGUMENT;
-  MergeParams p;
-  memset(&p, 0, sizeof(p));
+  MergeParams p = merge_params(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out,
+                               finalize != 0);
   if (order != nullptr) {
     bool seen[CP_MAX_MERGE_PARTS] = {false};
     for (int32_t i = 0; i < n_parts; ++i) {
@@ -417,21 +457,7 @@ cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t 
       seen[x] = true;
       p.order[i] = static_cast<uint16_t>(x);
     }
-  } else {
-    for (int32_t i = 0; i < n_parts; ++i) p.order[i] = static_cast<uint16_t>(i);
   }
-  p.batch = batch;
-  p.rows = rows;
-  p.heads = heads;
-  p.d = d;
-  p.n_parts = n_parts;
-  p.finalize = finalize != 0;
-  p.o_parts = o_parts;
-  p.m_parts = m_parts;
-  p.l_parts = l_parts;
-  p.o_out = o_out;
-  p.m_out = m_out;
-  p.l_out = l_out;
   return launch_merge(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
@@ -458,20 +484,8 @@ cp_status cp_merge_partials_tree(int64_t batch, int64_t rows, int64_t heads, int
   if (!aligned16(o_parts) || !aligned16(m_parts) || !aligned16(l_parts) || !aligned16(o_out) ||
       !aligned16(m_out) || !aligned16(l_out))
     return CP_ERR_INVALID_ARGUMENT;
-  MergeParams p;
-  memset(&p, 0, sizeof(p));
-  p.batch = batch;
-  p.rows = rows;
-  p.heads = heads;
-  p.d = d;
-  p.n_parts = n_parts;
-  p.finalize = finalize != 0;
-  p.o_parts = o_parts;
-  p.m_parts = m_parts;
-  p.l_parts = l_parts;
-  p.o_out = o_out;
-  p.m_out = m_out;
-  p.l_out = l_out;
+  const MergeParams p = merge_params(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out,
+                                     finalize != 0);
   return launch_merge_tree(p, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
@@ -499,30 +513,8 @@ cp_status cp_passq_decode(const cp_attn_desc* desc, const void* q, const void* k
   const int32_t splits = decode_splits_per_shard(*desc, sms);
   const size_t need = decode_workspace_bytes(*desc, splits);
   if (workspace_bytes < need) return CP_ERR_INVALID_ARGUMENT;
-  const int64_t n_parts = desc->cp * splits;
-  if (n_parts > CP_MAX_MERGE_PARTS) return CP_ERR_UNSUPPORTED;
-  float *o_parts = nullptr, *m_parts = nullptr, *l_parts = nullptr;
-  decode_workspace_sections(*desc, splits, workspace, &o_parts, &m_parts, &l_parts);
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (launch_decode_partials(*desc, splits, q, k, v, o_parts, m_parts, l_parts, s) != cudaSuccess)
-    return CP_ERR_CUDA;
-  // Three-quantity reduce: the LSE merge over the parts in shard order, finalised.
-  MergeParams p;
-  memset(&p, 0, sizeof(p));
-  p.batch = desc->b;
-  p.rows = 1;
-  p.heads = desc->h_q;
-  p.d = desc->d;
-  p.n_parts = static_cast<int32_t>(n_parts);
-  p.finalize = 1;
-  p.o_parts = o_parts;
-  p.m_parts = m_parts;
-  p.l_parts = l_parts;
-  p.o_out = out;
-  p.m_out = m_out;
-  p.l_out = l_out;
-  for (int32_t i = 0; i < p.n_parts; ++i) p.order[i] = static_cast<uint16_t>(i);
-  return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  return run_passq_decode(*desc, splits, q, k, v, workspace, out, m_out, l_out,
+                          static_cast<cudaStream_t>(cuda_stream));
 }
 
 cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const void* k, const void* v,
@@ -540,31 +532,10 @@ cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const
   int32_t splits = decode_splits_per_shard(*desc, sms);
   while (splits > 1 && decode_workspace_bytes(*desc, splits) > cap) splits /= 2;
   if (decode_workspace_bytes(*desc, splits) > cap) return CP_ERR_UNSUPPORTED;
-  const int64_t n_parts = desc->cp * splits;
-  if (n_parts > CP_MAX_MERGE_PARTS) return CP_ERR_UNSUPPORTED;
+  if (desc->cp * splits > CP_MAX_MERGE_PARTS) return CP_ERR_UNSUPPORTED;
   float* scratch = nullptr;
   if (decode_noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
-  float *o_parts = nullptr, *m_parts = nullptr, *l_parts = nullptr;
-  decode_workspace_sections(*desc, splits, scratch, &o_parts, &m_parts, &l_parts);
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (launch_decode_partials(*desc, splits, q, k, v, o_parts, m_parts, l_parts, s) != cudaSuccess)
-    return CP_ERR_CUDA;
-  MergeParams p;
-  memset(&p, 0, sizeof(p));
-  p.batch = desc->b;
-  p.rows = 1;
-  p.heads = desc->h_q;
-  p.d = desc->d;
-  p.n_parts = static_cast<int32_t>(n_parts);
-  p.finalize = 1;
-  p.o_parts = o_parts;
-  p.m_parts = m_parts;
-  p.l_parts = l_parts;
-  p.o_out = out;
-  p.m_out = m_out;
-  p.l_out = l_out;
-  for (int32_t i = 0; i < p.n_parts; ++i) p.order[i] = static_cast<uint16_t>(i);
-  return launch_merge(p, s) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  return run_passq_decode(*desc, splits, q, k, v, scratch, out, m_out, l_out, static_cast<cudaStream_t>(cuda_stream));
 }
 
 cp_status cp_selftest_wait_timeout(void* cuda_stream) {
