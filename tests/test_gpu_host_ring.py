@@ -103,3 +103,18 @@ def test_two_calls_in_a_row_on_one_stream_reuse_the_workspace():
     for q, k, v, (o, m, l), _ in runs:
         od, md, ld = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
         assert torch.equal(o, od.cpu()) and torch.equal(m, md.cpu()) and torch.equal(l, ld.cpu())
+
+
+def test_host_ring_at_full_size_equals_the_device_ring():
+    # The end-to-end call the benchmark times (GQA workload, pinned host buffers) gives
+    # the device-buffer launch's outputs bit for bit; that launch is held to the oracle
+    # on sampled rows at the same size in test_gpu_prefill.
+    w = synth.WORKLOADS["gqa"]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    o, m, l = _host_call(desc, q, k, v)
+    od, md, ld = run_ring(q, k, v, w["cp"], 0, w["cp"], EMIT | FIN)
+    assert torch.equal(m, md.cpu()) and torch.equal(l, ld.cpu())
+    assert torch.equal(o, od.cpu())
+    del q, k, v, od, md, ld
+    torch.cuda.empty_cache()
