@@ -568,7 +568,23 @@ def profile_case(name, steps):
     _build.build()
     cpa.load_library()
     stream = torch.cuda.current_stream()
-    if name == "decode-small":  # b8, 16 heads, d512, L8192, cp8: 2.1 GB of K/V
+    unit = "GB/s"
+    if name in ("ring-step", "ring-step-accumulate"):  # one ring step (t = 1) of the GQA workload
+        w = synth.WORKLOADS[WORKLOAD]
+        q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+        o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+        m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+        l = torch.empty_like(m)
+        desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+        mode = cpa.CP_MODE_EMIT
+        if name == "ring-step-accumulate":  # into the step-0 triple
+            cpa.cp_ring_step_partial_attn(desc, 0, 1, q, k, v, o, m, l, cpa.CP_MODE_EMIT, stream)
+            mode = cpa.CP_MODE_ACCUMULATE
+        fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, mode, stream)  # noqa: E731
+        C = w["S"] // (2 * w["cp"])
+        work = 4 * w["b"] * w["h_q"] * w["d"] * w["cp"] * 2 * C * C / 1e3  # so that work / s / 1e9 is TFLOP/s
+        unit = "TFLOP/s"
+    elif name == "decode-small":  # b8, 16 heads, d512, L8192, cp8: 2.1 GB of K/V
         b, L, h, d, cp = 8, 8192, 16, 512, 8
         q, k, v = synth.decode_inputs(b, L, h, h, d, seed=7)
         desc = cpa.make_desc(b, L, h, h, d, cp, 1.0 / math.sqrt(d), 0)
@@ -609,7 +625,7 @@ def profile_case(name, steps):
     for _ in range(3):
         fn()
     ms = _events_time(fn, steps, stream)
-    print(json.dumps({"case": name, "ms": round(ms, 4), "GB/s": round(work / (ms * 1e-3) / 1e9, 1)}))
+    print(json.dumps({"case": name, "ms": round(ms, 4), unit: round(work / (ms * 1e-3) / 1e9, 1)}))
 
 
 def main():
@@ -623,7 +639,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--case", choices=["decode-small", "decode-shared-kv", "merge", "merge-tree"], default=None,
+    ap.add_argument("--case", choices=["ring-step", "ring-step-accumulate", "decode-small", "decode-shared-kv", "merge",
+                                       "merge-tree"], default=None,
                     help="time one kernel on a capture-sized case (for ncu) instead of the benchmark")
     args = ap.parse_args()
     if args.case is not None:
