@@ -170,7 +170,9 @@ CPATTN_API cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t
  * units' computation.  The call is ordered on `cuda_stream`: it starts after the
  * work queued there before it, later work queued there starts after its last
  * copy, and the workspace is in use until then.  The host is not blocked:
- * synchronise `cuda_stream` before reading the outputs.
+ * synchronise `cuda_stream` before reading the outputs.  Calls from several host
+ * threads are safe with one workspace each; on one device they share the library's
+ * streams, so their copies and launches interleave rather than run side by side.
  * Errors: as cp_ring_step_partial_attn, plus a NULL host pointer or a misaligned
  * or too small workspace -> CP_ERR_INVALID_ARGUMENT; a failed copy, launch or
  * stream/event call -> CP_ERR_CUDA.
