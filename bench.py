@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "595ad7ad90c203fa", "bytes": 2163691776}
+RING_TRAFFIC = {"sha256_prefix": "7f68bd06f04fcaa8", "bytes": 894163712}
 
 
 def ring_traffic():
