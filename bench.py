@@ -72,7 +72,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "7f68bd06f04fcaa8", "bytes": 894163712}
+RING_TRAFFIC = {"sha256_prefix": "8be4290917438b4c", "bytes": 892329984}
 
 
 def ring_traffic():

@@ -219,17 +219,19 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.tpc;  // query tiles of the selected chunks
   // Units (sequence, kv head) in groups whose K/V fits in L2; within a group, the
   // latest chunk (most keys) first, then the group's head pairs.
-  const int64_t upg = p.b * p.h_kv / p.unit_groups;  // units per group
-  const int64_t per_tile = upg * p.ppg;
-  const int64_t per_group = int64_t(n_qt) * per_tile;
-  const int64_t g = int64_t(blockIdx.x) / per_group;
-  const int64_t idx = int64_t(blockIdx.x) % per_group;
-  const int32_t gq = n_qt - 1 - int32_t(idx / per_tile);
-  const int64_t bp = idx % per_tile;
-  const int32_t i = int32_t(bp % p.ppg);
-  const int64_t unit = g * upg + bp / p.ppg;
-  it.bi = int32_t(unit / p.h_kv);
-  it.kvh = int32_t(unit % p.h_kv);
+  // The launch has fewer than 2^31 items, so every index here fits 32 bits.
+  const int32_t upg = int32_t(p.b * p.h_kv) / p.unit_groups;  // units per group
+  const int32_t per_tile = upg * p.ppg;
+  const int32_t per_group = n_qt * per_tile;
+  const int32_t g = int32_t(blockIdx.x) / per_group;
+  const int32_t idx = int32_t(blockIdx.x) - g * per_group;
+  const int32_t gq = n_qt - 1 - idx / per_tile;
+  const int32_t bp = idx - (n_qt - 1 - gq) * per_tile;
+  const int32_t u = bp / p.ppg;
+  const int32_t i = bp - u * p.ppg;
+  const int32_t unit = g * upg + u;
+  it.bi = unit / int32_t(p.h_kv);
+  it.kvh = unit - it.bi * int32_t(p.h_kv);
   it.h0 = it.kvh * p.group + 2 * i;
   it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
   // a-th selected chunk in ascending order.  Balanced: the ranks' head chunks
@@ -811,11 +813,13 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
     // unit each): a group's K/V then stays in L2 while its CTAs run, next to the Q and O
     // streams.  40 MB measured best (0.40 GB of DRAM reads per GQA launch, 0.56 GB at
     // 70 MB, 1.68 GB ungrouped).
+    // One ring step needs no grouping: the CTAs that share a K/V block lie within about
+    // two waves of each other in the plain order (grouping measured 1 % slower there).
     const int64_t units = d.b * d.h_kv;
     const int64_t unit_bytes = d.S * d.d * 2 * 2;
     const int64_t budget = kL2UnitBudget;
     int64_t groups = 1;
-    while (groups < units && (units / groups) * unit_bytes > budget) {
+    while (step_end - step_begin > 1 && groups < units && (units / groups) * unit_bytes > budget) {
       int64_t next = groups + 1;
       while (units % next != 0) ++next;
       groups = next;
