@@ -309,3 +309,33 @@ def test_full_size_workload_sampled_rows(name):
         assert np.abs(lse - (ref_m[0] + np.log(ref_l[0]))).max() <= LSE_ABS
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
+
+
+def test_grouped_item_order_writes_every_row_once():
+    # 2 sequences x 8 kv heads of 8.4 MB of K/V each: the full ring runs its CTAs in four
+    # groups of (sequence, kv head) units.  Every output row of every head must be written
+    # (NaN-filled buffers) and sampled rows of heads in every group match the oracle.
+    b, S, hq, hkv, d, cp = 2, 16384, 32, 8, 128, 8
+    q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=77)
+    o = torch.full((b, S, hq, d), float("nan"), dtype=torch.float32, device="cuda")
+    m = torch.full((b, hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    l = torch.full((b, hq, S), float("nan"), dtype=torch.float32, device="cuda")
+    run_ring(q, k, v, cp, 0, cp, EMIT | FIN, (o, m, l))
+    assert torch.isfinite(o).all() and torch.isfinite(m).all() and torch.isfinite(l).all()
+    assert (l > 0).all()
+    rows = synth.sample_rows(S, cp, 8, seed=77)
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d)
+    for bi in range(b):
+        for h in (0, 9, 18, 31):  # kv heads 0, 2, 4, 7
+            kh = h // g
+            qfull = np.zeros((1, S, 1, d))
+            qfull[0, rows] = f64(q[bi, rows, h:h + 1])
+            ks = f64(k[bi, :, kh:kh + 1])[None]
+            vs = f64(v[bi, :, kh:kh + 1])[None]
+            ref_out, ref_m, ref_l = OA.causal_attention_rows(qfull, ks, vs, scale, 0, [0], rows)
+            assert_out_close(o[bi, rows, h].cpu().numpy(), ref_out[0], f"seq {bi} head {h}")
+            lse = (m[bi, h, rows] + torch.log(l[bi, h, rows])).cpu().numpy()
+            assert np.abs(lse - (ref_m[0] + np.log(ref_l[0]))).max() <= LSE_ABS
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
