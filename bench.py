@@ -17,7 +17,9 @@ during the timed region, and secondary lines for pass-Q decode (GB/s) and the
 LSE merge (GB/s).
 
 ``--impl reference`` times the CPU oracle (fp64, test infrastructure) on a
-bounded row sample of the same workload on the host cores.
+bounded row sample of the same workload on the host cores.  The decode and merge
+secondary lines carry the oracle timed the same way on a bounded sample of their
+own inputs (unless --skip-cpu).
 """
 
 from __future__ import annotations
@@ -187,6 +189,52 @@ def oracle_sample_tasks(w, q, k, v, rows_per_head, heads, seed):
     return tasks
 
 
+def _oracle_decode_task(args):
+    """One worker: pass-Q decode of one (sequence, head) over all its keys (fp64 oracle)."""
+    qbits, kbits, vbits, scale = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from oracle import attention as OA
+    q = oracle.bf16_bits_to_f64(qbits)   # [d]
+    k = oracle.bf16_bits_to_f64(kbits)   # [L, d]
+    v = oracle.bf16_bits_to_f64(vbits)
+    t0 = time.perf_counter()
+    OA.decode_attention(q[None, None], k[None, :, None], v[None, :, None], scale)
+    dt = time.perf_counter() - t0
+    return 2 * k.size * 2, dt  # the bf16 K and V bytes this decode reads
+
+
+def _oracle_merge_task(args):
+    """One worker: the fold of n parts over some rows of one head (fp64 oracle)."""
+    m_parts, l_parts, o_parts = args     # [n, R], [n, R], [n, R, d] fp32
+    sys.path.insert(0, ROOT)
+    from oracle import ring as OR
+    n, R, d = o_parts.shape
+    parts = [(m_parts[p].astype(np.float64), l_parts[p].astype(np.float64), o_parts[p].astype(np.float64))
+             for p in range(n)]
+    t0 = time.perf_counter()
+    OR.merge_in_order(parts)
+    dt = time.perf_counter() - t0
+    return (n + 1) * R * (d + 2) * 4, dt  # the parts read and the triple written, in fp32 bytes
+
+
+def run_oracle_each(fn, tasks):
+    """Runs one task per single-threaded spawn worker, all at once; each worker times
+    its own task, so moving the inputs to the workers is not counted.  Returns the
+    tasks' bytes over the slowest worker's time (bytes/s) and that time."""
+    import multiprocessing as mp
+    os.environ["CPATTN_ORACLE_WORKER"] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(len(tasks)) as pool:
+            pool.map(_oracle_warm, range(len(tasks)))
+            res = pool.map(fn, tasks)
+    finally:
+        os.environ.pop("CPATTN_ORACLE_WORKER", None)
+    slowest = max(r[1] for r in res)
+    return sum(r[0] for r in res) / slowest, slowest
+
+
 def _oracle_warm(_):
     sys.path.insert(0, ROOT)
     import oracle  # noqa: F401
@@ -353,7 +401,7 @@ def bench_ours(args, rank, world, dist):
 
     secondary = {}
     if not args.skip_secondary and rank == 0:
-        secondary = secondary_lines(cpa, synth, peaks, stream)
+        secondary = secondary_lines(cpa, synth, peaks, stream, cpu_legs=not args.skip_cpu)
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -380,7 +428,7 @@ def bench_ours(args, rank, world, dist):
     return line
 
 
-def secondary_lines(cpa, synth, peaks, stream):
+def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
     import torch
     out = {}
     # one ring step (t = 1) of all cp virtual ranks on the GQA workload, EMIT: the spec's
@@ -473,6 +521,15 @@ def secondary_lines(cpa, synth, peaks, stream):
     out["decode"] = {"workload": "pass-Q decode: b8, 16 heads, d512, L131072, cp8", "value": round(gbs, 1),
                      "unit": "GB/s", "ms": round(ms, 4), "bytes": decode_bytes(w), "peak": peaks["hbm_gbs"],
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": 2}
+    if cpu_legs:  # the oracle on 4 (sequence, head) pairs of the same inputs, one per worker
+        pairs = [(0, 0), (3, 5), (5, 10), (7, 15)]
+        tasks = [(synth.bf16_bits(q[bi, h]), synth.bf16_bits(k[bi, :, h]), synth.bf16_bits(v[bi, :, h]),
+                  1.0 / math.sqrt(w["d"])) for bi, h in pairs]
+        rate, slowest = run_oracle_each(_oracle_decode_task, tasks)
+        out["decode"]["cpu_baseline"] = {
+            "value": round(rate / 1e9, 4), "unit": "GB/s", "cores": len(tasks), "kind": "oracle",
+            "sample": f"{len(tasks)} (sequence, head) pairs, all 131072 keys each (fp64 numpy decode), one per "
+                      f"single-threaded spawn worker; slowest worker {slowest:.2f} s"}
     del q, k, v, ws
     torch.cuda.empty_cache()
     # pass-Q decode with 16 query heads sharing one 512-wide K/V head (MQA / MLA-style), tensor cores
@@ -511,6 +568,15 @@ def secondary_lines(cpa, synth, peaks, stream):
     out["merge"] = {"workload": "LSE merge: 32 parts x 64 heads x 4096 rows x 128", "value": round(gbs, 1),
                     "unit": "GB/s", "ms": round(ms, 4), "bytes": merge_bytes(w), "peak": peaks["hbm_gbs"],
                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    if cpu_legs:  # the oracle's fold over all rows of 4 heads of the same parts, one head per worker
+        R = w["rows"]
+        tasks = [(pm[:, 0, h, :R].cpu().numpy(), pl[:, 0, h, :R].cpu().numpy(), po[:, 0, :R, h].cpu().numpy())
+                 for h in (0, 21, 42, 63)]
+        rate, slowest = run_oracle_each(_oracle_merge_task, tasks)
+        out["merge"]["cpu_baseline"] = {
+            "value": round(rate / 1e9, 4), "unit": "GB/s", "cores": len(tasks), "kind": "oracle",
+            "sample": f"{len(tasks)} heads x {R} rows x {w['parts']} parts (fp64 numpy fold), one head per "
+                      f"single-threaded spawn worker; slowest worker {slowest:.3f} s"}
     # the same 32 parts reduced as the log-depth halving tree (5 levels of pairwise
     # merges), computed in one pass
     nbytes = cpa.cp_merge_tree_workspace_bytes(1, w["rows"], w["heads"], w["d"], w["parts"])
