@@ -236,8 +236,11 @@ def test_decode_matches_oracle(case):
 
 
 # Query heads sharing one K/V head (MQA / MLA-style): the tensor-core decode kernel.
+# The last two shapes split each shard into unequal key ranges (5 and 4 tiles), the
+# second ending on a ragged tile.
 MQA_SMALL = [(2, 4096, 16, 1, 512, 4), (1, 2048, 32, 1, 128, 2), (1, 3000, 16, 1, 256, 3),
-             (2, 384, 32, 2, 128, 1), (1, 200, 16, 1, 512, 2), (3, 8192, 16, 1, 128, 8)]
+             (2, 384, 32, 2, 128, 1), (1, 200, 16, 1, 512, 2), (3, 8192, 16, 1, 128, 8),
+             (1, 2100, 16, 1, 256, 2), (1, 4200, 32, 1, 128, 4)]
 
 
 @pytest.mark.parametrize("case", MQA_SMALL, ids=[str(c) for c in MQA_SMALL])
