@@ -506,6 +506,27 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
                            "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
+    # tiny prefill: b1, 4/4 heads, d64, S1024, cp2 (0.54 GFLOP).  A few CTAs per head and
+    # 1 MB of inputs that stay in L2: launch- and latency-bound, reported as measured.
+    w = synth.WORKLOADS["tiny"]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+    l = torch.empty_like(m)
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    mode = cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE
+    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, stream)  # noqa: E731
+    for _ in range(10):
+        fn()
+    ms = _events_time(fn, 200, stream)
+    tf = prefill_flops(w) / (ms * 1e-3) / 1e12
+    out["prefill_tiny"] = {"workload": "prefill ring attention, tiny: b1, 4/4 heads, d64, S1024, cp2 "
+                                       "(inputs in L2; launch- and latency-bound)",
+                           "value": round(tf, 2), "unit": "TFLOP/s", "us": round(ms * 1e3, 2),
+                           "flops": prefill_flops(w), "peak": peaks["bf16_tflops"],
+                           "frac": round(tf / peaks["bf16_tflops"], 4)}
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
     # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)
     w = synth.WORKLOADS["decode"]
     q, k, v = synth.decode_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], seed=w["seed"])
