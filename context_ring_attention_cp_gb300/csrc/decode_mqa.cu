@@ -542,8 +542,8 @@ bool decode_mqa_supported(const cp_attn_desc& d) {
 }
 
 // Key ranges per shard.  Each candidate count (ranges of at least four tiles, at most
-// CP_MAX_MERGE_PARTS parts) is scored by walking the items as the kernel's grid
-// does: the busiest CTA's tiles, plus one tile per item for the switch between items
+// CP_MAX_MERGE_PARTS parts) is scored as the kernel's grid walks the items: the
+// busiest CTA's tiles, plus one tile per item for the switch between items
 // (measured: 19 ranges, 0.2 % from even, ran slower than 16 ranges, 4 % from even).
 // The lowest score wins, the fewer ranges on a tie.
 int32_t decode_mqa_splits(const cp_attn_desc& d, int sm_count) {
@@ -555,16 +555,13 @@ int32_t decode_mqa_splits(const cp_attn_desc& d, int sm_count) {
   for (int64_t s = 1; s <= tiles && d.cp * s <= CP_MAX_MERGE_PARTS; ++s) {
     if (s > 1 && tiles / s < 4) break;
     const int64_t items = s * units;
-    if (items > (int64_t(1) << 24)) break;  // the walk below stays cheap
     const int64_t grid = items < sms ? items : sms;
     const int64_t base = tiles / s, rem = tiles % s;
-    int64_t worst = 0;
-    for (int64_t c = 0; c < grid; ++c) {
-      int64_t sum = 0;
-      for (int64_t i = c; i < items; i += grid) sum += base + ((i / units) < rem ? 1 : 0);
-      if (sum > worst) worst = sum;
-    }
-    const double score = double(worst) + double((items + grid - 1) / grid);
+    // CTA c walks items c, c + grid, ...; the first rem * units items are one tile
+    // longer.  Both counts fall with c, so CTA 0 is the busiest.
+    const int64_t per_cta = (items + grid - 1) / grid;
+    const int64_t worst = per_cta * base + (rem * units + grid - 1) / grid;
+    const double score = double(worst) + double(per_cta);
     if (s == 1 || score < best_score) {
       best = s;
       best_score = score;
