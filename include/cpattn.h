@@ -240,9 +240,11 @@ CPATTN_API cp_status cp_passq_workspace_bytes(const cp_attn_desc* desc, size_t* 
  * Pass-Q decode (Terms table row "Pass-Q"; use-case decode paragraph; pass-Q
  * paragraph of the Algorithm/formulas section).  One query per sequence is
  * scored against cp KV shards: shard s holds keys [s*L/cp, (s+1)*L/cp) with
- * L = desc->S; every key is visible.  Each shard is further split into equal
- * key ranges so the whole GPU streams K/V; every range writes a partial triple to
- * `workspace`, then the three-quantity reduce (the LSE merge, in shard order)
+ * L = desc->S; every key is visible.  Each shard is further split into key
+ * ranges so the whole GPU streams K/V (equal ranges for the streaming kernel; whole
+ * 128-key tiles of at most one tile's difference for the shared-K/V kernel, the
+ * count chosen so that the SMs get even work); every range writes a partial triple
+ * to `workspace`, then the three-quantity reduce (the LSE merge, in shard order)
  * writes
  *   out   [b, h_q, d] fp32 = O / l,   m_out, l_out [b, h_q] fp32 (each nullable).
  * q [b, h_q, d] bf16; k, v [b, L, h_kv, d] bf16.  The query dispatch of the spec
