@@ -8,8 +8,8 @@
 // same quantity as a left fold of pairwise merges; only rounding differs.
 //
 // HBM-bound: each (batch, head, row) reads n_parts x (d + 2) floats and writes
-// d + 2.  One CTA covers 32 consecutive rows of one (batch, head): it first
-// stages the 2 x n_parts x 32 scalars (m, l) with coalesced loads into shared
+// d + 2.  One CTA covers kRowsPerCta consecutive rows of one (batch, head): it first
+// stages the 2 x n_parts x kRowsPerCta scalars (m, l) with coalesced loads into shared
 // memory, then each warp streams the O rows of its rows part by part, lanes
 // owning float4 slices of d, with eight (d <= 128) down to two (d = 512) parts of loads
 // in flight per lane.
@@ -23,7 +23,7 @@
 namespace cpattn {
 namespace {
 
-constexpr int kRowsPerCta = 32;
+constexpr int kRowsPerCta = 16;  // 0.680 ms on the merge-stress workload against 0.684 at 32
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(c
   constexpr int kUnroll = (8 / NCH) < 2 ? 2 : (8 / NCH);  // parts in flight per lane
   extern __shared__ float smem[];
   const int n_parts = p.n_parts;
-  float* sm_m = smem;                          // [n_parts][32] in fold order
-  float* sm_l = smem + n_parts * kRowsPerCta;  // [n_parts][32]
+  float* sm_m = smem;                          // [n_parts][kRowsPerCta] in fold order
+  float* sm_l = smem + n_parts * kRowsPerCta;  // [n_parts][kRowsPerCta]
 
   const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t tile = blockIdx.x;
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(c
   const int64_t bi = bh / p.heads;
   const int64_t row0 = rb * kRowsPerCta;
 
-  // Stage m and l of every part for the 32 rows (consecutive threads -> consecutive rows).
+  // Stage m and l of every part for the CTA's rows (consecutive threads -> consecutive rows).
   for (int idx = threadIdx.x; idx < n_parts * kRowsPerCta; idx += kThreads) {
     const int kpos = idx / kRowsPerCta;
     const int r = idx % kRowsPerCta;
