@@ -220,7 +220,7 @@ def _decode(q, k, v, cp):
 
 DECODE_SMALL = [(2, 4096, 4, 4, 128, 4), (3, 2048, 8, 2, 64, 2), (1, 1024, 2, 1, 256, 1),
                 (2, 8192, 16, 16, 512, 8), (1, 3000, 4, 2, 512, 3), (2, 96, 4, 4, 128, 8),
-                (1, 12, 2, 2, 64, 4)]
+                (1, 12, 2, 2, 64, 4), (2, 8, 4, 2, 128, 8)]  # the last: one key per shard
 
 
 @pytest.mark.parametrize("case", DECODE_SMALL, ids=[str(c) for c in DECODE_SMALL])
@@ -236,11 +236,12 @@ def test_decode_matches_oracle(case):
 
 
 # Query heads sharing one K/V head (MQA / MLA-style): the tensor-core decode kernel.
-# The last two shapes split each shard into unequal key ranges (5 and 4 tiles), the
-# second ending on a ragged tile.
+# Shapes 7 and 8 split each shard into unequal key ranges (5 and 4 tiles), the second
+# ending on a ragged tile; the last two hold one key per shard.
 MQA_SMALL = [(2, 4096, 16, 1, 512, 4), (1, 2048, 32, 1, 128, 2), (1, 3000, 16, 1, 256, 3),
              (2, 384, 32, 2, 128, 1), (1, 200, 16, 1, 512, 2), (3, 8192, 16, 1, 128, 8),
-             (1, 2100, 16, 1, 256, 2), (1, 4200, 32, 1, 128, 4)]
+             (1, 2100, 16, 1, 256, 2), (1, 4200, 32, 1, 128, 4),
+             (1, 8, 16, 1, 128, 8), (2, 2, 32, 1, 256, 2)]  # one key per shard
 
 
 @pytest.mark.parametrize("case", MQA_SMALL, ids=[str(c) for c in MQA_SMALL])
