@@ -322,3 +322,22 @@ def test_decode_rejects_small_workspace():
     out = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(cpa.CpError):
         cpa.cp_passq_decode(desc, q, k, v, ws, need - 4, out)
+
+
+@pytest.mark.parametrize("case", [(2, 4096, 4, 4, 128, 4), (2, 4096, 16, 1, 256, 4)], ids=["streaming", "shared_kv"])
+def test_decode_scale_is_the_one_passed(case):
+    # Both decode kernels against the oracle at a scale other than 1/sqrt(d).
+    b, L, hq, hkv, d, cp = case
+    scale = 0.7 / math.sqrt(d)
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=55)
+    desc = cpa.make_desc(b, L, hq, hkv, d, cp, scale, 0)
+    ws_bytes = cpa.cp_passq_workspace_bytes(desc)
+    ws = torch.empty(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    mo = torch.empty((b, hq), dtype=torch.float32, device="cuda")
+    lo = torch.empty_like(mo)
+    cpa.cp_passq_decode(desc, q, k, v, ws, ws_bytes, out, mo, lo)
+    assert cpa.cp_take_device_status() == 0
+    ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), scale)
+    assert_out_close(out.cpu().numpy(), ref_out, f"decode scale {case}")
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS

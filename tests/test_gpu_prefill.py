@@ -339,3 +339,29 @@ def test_grouped_item_order_writes_every_row_once():
             assert np.abs(lse - (ref_m[0] + np.log(ref_l[0]))).max() <= LSE_ABS
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("scale", [0.3, 2.0 / math.sqrt(128)])
+def test_softmax_scale_is_the_one_passed(scale):
+    # The scale is an explicit argument: a kernel that used 1/sqrt(d) regardless would
+    # fail here (fused ring and one EMIT step, against the oracle at the same scale).
+    b, S, hq, hkv, d, cp = 1, 1024, 4, 2, 128, 4
+    q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=44)
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, scale, 1)
+    o, m, l = ring_buffers(b, S, hq, d)
+    cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, o, m, l, EMIT | FIN)
+    assert cpa.cp_take_device_status() == 0
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    ref_out, ref_m, ref_l, _ = OA.full_causal_attention(qf, kf, vf, scale)
+    assert_out_close(o.cpu().numpy(), ref_out, f"scale {scale}")
+    assert np.abs(m.cpu().numpy() - ref_m).max() <= LSE_ABS
+    o1, m1, l1 = ring_buffers(b, S, hq, d)
+    cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o1, m1, l1, EMIT)
+    assert cpa.cp_take_device_status() == 0
+    m1n, l1n = m1.cpu().numpy(), l1.cpu().numpy()
+    for r in range(cp):
+        rows, rm, rl, ro = OR.ring_step_triple(qf, kf, vf, scale, cp, r, 1)
+        live = ~np.isneginf(rm)
+        gm, gl = m1n[:, :, rows], l1n[:, :, rows]
+        assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
+        assert np.abs((gm + np.log(np.where(live, gl, 1)))[live] - (rm + np.log(np.where(live, rl, 1)))[live]).max() <= LSE_ABS
