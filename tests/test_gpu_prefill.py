@@ -337,7 +337,16 @@ def test_grouped_item_order_writes_every_row_once():
             assert_out_close(o[bi, rows, h].cpu().numpy(), ref_out[0], f"seq {bi} head {h}")
             lse = (m[bi, h, rows] + torch.log(l[bi, h, rows])).cpu().numpy()
             assert np.abs(lse - (ref_m[0] + np.log(ref_l[0]))).max() <= LSE_ABS
-    del q, k, v, o, m, l
+    # one launch per rank (each grouped the same way over its own items) writes exactly
+    # that rank's rows, and together they equal the all-ranks launch bit for bit
+    parts = tuple(torch.full_like(x, float("nan")) for x in (o, m, l))
+    for r in range(cp):
+        _run_ranks(q, k, v, cp, cpa.CP_LAYOUT_BALANCED, r, r + 1, 0, cp, EMIT | FIN, parts)
+        mine = OR.rank_rows(S, cp, r, "balanced")
+        assert torch.isfinite(parts[0][:, mine]).all(), f"rank {r} left rows unwritten"
+    for x, y in zip(parts, (o, m, l)):
+        assert torch.equal(x, y)
+    del q, k, v, o, m, l, parts
     torch.cuda.empty_cache()
 
 
