@@ -374,3 +374,31 @@ def test_softmax_scale_is_the_one_passed(scale):
         gm, gl = m1n[:, :, rows], l1n[:, :, rows]
         assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
         assert np.abs((gm + np.log(np.where(live, gl, 1)))[live] - (rm + np.log(np.where(live, rl, 1)))[live]).max() <= LSE_ABS
+
+
+def test_per_step_accumulate_chain_at_full_size():
+    # How the method runs on cp devices: one launch per ring step, each merged into the
+    # running triple, the last one normalising (GQA workload, full size).  P is rounded
+    # to bf16 against each launch's own reference, so the chain and the fused ring agree
+    # to that rounding; sampled rows are held to the oracle.
+    w = synth.WORKLOADS["gqa"]
+    b, S, hq, hkv, d, cp = w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"]
+    q, k, v = synth.prefill_inputs(b, S, hq, hkv, d, std=w["std"], seed=w["seed"])
+    chain = ring_buffers(b, S, hq, d, identity=True)
+    for t in range(cp):
+        run_ring(q, k, v, cp, t, t + 1, ACC | (FIN if t == cp - 1 else 0), chain)
+    fused = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    assert torch.equal(chain[1], fused[1])  # the max is exact in any grouping
+    assert (chain[0] - fused[0]).abs().max().item() <= 5e-3
+    rows = synth.sample_rows(S, cp, 16, seed=w["seed"] + 1)
+    g = hq // hkv
+    scale = 1.0 / math.sqrt(d)
+    for h in (3, 30):
+        kh = h // g
+        qfull = np.zeros((1, S, 1, d))
+        qfull[0, rows] = f64(q[0, rows, h:h + 1])
+        ref_out, _, _ = OA.causal_attention_rows(qfull, f64(k[0, :, kh:kh + 1])[None], f64(v[0, :, kh:kh + 1])[None],
+                                                 scale, 0, [0], rows)
+        assert_out_close(chain[0][0, rows, h].cpu().numpy(), ref_out[0], f"chain head {h}")
+    del q, k, v, chain, fused
+    torch.cuda.empty_cache()
