@@ -463,6 +463,23 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
                     "of the GQA prefill workload",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
         "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+    # the whole ring as cp launches of one step each (the first EMIT, then ACCUMULATE, the
+    # last normalising), as the steps run when each rank launches per step
+    def chain():
+        for t in range(w["cp"]):
+            md = cpa.CP_MODE_EMIT if t == 0 else cpa.CP_MODE_ACCUMULATE
+            if t == w["cp"] - 1:
+                md |= cpa.CP_MODE_FINALIZE
+            cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, o, m, l, md, stream)
+    for _ in range(3):
+        chain()
+    ms = _events_time(chain, 10, stream)
+    tf = prefill_flops(w) / (ms * 1e-3) / 1e12
+    out["prefill_per_step_chain"] = {
+        "workload": "the GQA prefill ring as 8 single-step launches (EMIT, ACCUMULATE..., the last "
+                    "FINALIZE) instead of one fused launch",
+        "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": prefill_flops(w),
+        "launches": w["cp"], "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # per-virtual-rank work under the balanced (method) and sequential (plain) layouts:
