@@ -311,11 +311,13 @@ def test_full_size_workload_sampled_rows(name):
     torch.cuda.empty_cache()
 
 
-def test_grouped_item_order_writes_every_row_once():
-    # 2 sequences x 8 kv heads of 8.4 MB of K/V each: the full ring runs its CTAs in four
-    # groups of (sequence, kv head) units.  Every output row of every head must be written
-    # (NaN-filled buffers) and sampled rows of heads in every group match the oracle.
-    b, S, hq, hkv, d, cp = 2, 16384, 32, 8, 128, 8
+@pytest.mark.parametrize("S", [16384, 16000], ids=["whole_tiles", "ragged_tiles"])
+def test_grouped_item_order_writes_every_row_once(S):
+    # 2 sequences x 8 kv heads of about 8 MB of K/V each: the full ring runs its CTAs in
+    # four groups of (sequence, kv head) units (S 16000: chunks of 7 whole tiles and one of
+    # 104 rows).  Every output row of every head must be written (NaN-filled buffers) and
+    # sampled rows of heads in every group match the oracle.
+    b, hq, hkv, d, cp = 2, 32, 8, 128, 8
     q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=77)
     o = torch.full((b, S, hq, d), float("nan"), dtype=torch.float32, device="cuda")
     m = torch.full((b, hq, S), float("nan"), dtype=torch.float32, device="cuda")
