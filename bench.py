@@ -537,9 +537,19 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
         fn()
     ms = _events_time(fn, 200, stream)
     tf = prefill_flops(w) / (ms * 1e-3) / 1e12
+    # the same launches replayed from a CUDA graph (20 per graph): no host launch cost
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=torch.cuda.Stream()):  # captured off the default stream
+        for _ in range(20):
+            cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, torch.cuda.current_stream())
+    for _ in range(3):
+        graph.replay()
+    ms_graph = _events_time(graph.replay, 10, stream) / 20
     out["prefill_tiny"] = {"workload": "prefill ring attention, tiny: b1, 4/4 heads, d64, S1024, cp2 "
                                        "(inputs in L2; launch- and latency-bound)",
                            "value": round(tf, 2), "unit": "TFLOP/s", "us": round(ms * 1e3, 2),
+                           "us_in_cuda_graph": round(ms_graph * 1e3, 2),
                            "flops": prefill_flops(w), "peak": peaks["bf16_tflops"],
                            "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
