@@ -102,6 +102,8 @@ struct RingParams {
   int32_t C;          // chunk length S / (2 cp)
   int32_t cp;
   int32_t tpc;        // query tiles per chunk
+  int32_t row_pairs;  // 1: a CTA takes two consecutive query tiles of one head (odd group)
+  int32_t ipc;        // work items per chunk along its rows: tpc, or ceil(tpc / 2) with row_pairs
   int32_t n_pairs;    // head pairs per batch entry
   int32_t ppg;        // head pairs per kv group
   int32_t group;      // h_q / h_kv
@@ -207,16 +209,21 @@ struct KvCursor {
   }
 };
 
+// One CTA's work: query tile A and, when has_b, tile B, which share every K/V tile.
+// Tile B is the next query head of the kv group (dh = 1, same rows; even groups) or
+// the next 128 rows of the same head (drow = BM; odd groups, so that no head is left
+// without a partner).
 struct Item {
   int32_t bi, h0, has_b, kvh;
   int32_t c_q, r, q_row0, q_rows;
+  int32_t dh, drow, q_rows_b, q_last;  // tile B's offsets and rows; the last row of either tile
 };
 
 template <int LAYOUT>
 __device__ __forceinline__ Item decode_item(const RingParams& p) {
   Item it;
   const int32_t nr = p.rank_end - p.rank_begin;
-  const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.tpc;  // query tiles of the selected chunks
+  const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.ipc;  // row items of the selected chunks
   // Units (sequence, kv head) in groups whose K/V fits in L2; within a group, the
   // latest chunk (most keys) first, then the group's head pairs.
   // The launch has fewer than 2^31 items, so every index here fits 32 bits.
@@ -232,14 +239,13 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t unit = g * upg + u;
   it.bi = unit / int32_t(p.h_kv);
   it.kvh = unit - it.bi * int32_t(p.h_kv);
-  it.h0 = it.kvh * p.group + 2 * i;
-  it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
+  it.h0 = it.kvh * p.group + (p.row_pairs ? i : 2 * i);
   // a-th selected chunk in ascending order.  Balanced: the ranks' head chunks
   // [rank_begin, rank_end) then their tail chunks [2cp-rank_end, 2cp-rank_begin);
   // sequential: chunks [2 rank_begin, 2 rank_end).  With one chunk per rank selected,
   // only the head (first) or only the tail (second) chunks, in ascending order.
-  int32_t a = gq / p.tpc;
-  const int32_t kq = gq % p.tpc;
+  int32_t a = gq / p.ipc;
+  const int32_t kq = gq % p.ipc;
   if (p.chunks == kRingSecondChunk) a += nr;
   if (LAYOUT == CP_LAYOUT_SEQUENTIAL) {
     it.c_q = (p.chunks == kRingBothChunks) ? 2 * p.rank_begin + a
@@ -249,8 +255,22 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
     it.c_q = (a < nr) ? p.rank_begin + a : 2 * p.cp - p.rank_end + (a - nr);
     it.r = (it.c_q < p.cp) ? it.c_q : 2 * p.cp - 1 - it.c_q;
   }
-  it.q_row0 = it.c_q * p.C + BM * kq;
-  it.q_rows = min(BM, p.C - BM * kq);
+  const int32_t tile0 = p.row_pairs ? 2 * kq : kq;  // first query tile of the item in its chunk
+  it.q_row0 = it.c_q * p.C + BM * tile0;
+  it.q_rows = min(BM, p.C - BM * tile0);
+  if (p.row_pairs) {
+    it.dh = 0;
+    it.drow = BM;
+    it.q_rows_b = max(0, min(BM, p.C - BM * (tile0 + 1)));
+    it.has_b = it.q_rows_b > 0 ? 1 : 0;
+    it.q_last = it.has_b ? it.q_row0 + BM + it.q_rows_b - 1 : it.q_row0 + it.q_rows - 1;
+  } else {
+    it.dh = 1;
+    it.drow = 0;
+    it.q_rows_b = it.q_rows;
+    it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
+    it.q_last = it.q_row0 + it.q_rows - 1;
+  }
   return it;
 }
 
@@ -310,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   const bool skip = *abort_flag != 0;
   // Number of KV tiles this query tile visits over the step range.
   const int32_t n_kv = KvCursor<LAYOUT>::count(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C,
-                                               it.q_row0 + it.q_rows - 1);
+                                               it.q_last);
   const int n_q = 1 + it.has_b;
 
   // Register split (launched with 168 per thread, 64,512 in all): the producer /
@@ -331,28 +351,30 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       for (int tt = 0; tt < n_q; ++tt)
         for (int sl = 0; sl < K::kSlabs; ++sl)
           tma_load_4d_hint(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
-                           it.h0 + tt, it.q_row0, it.bi, pol_once);
+                           it.h0 + tt * it.dh, it.q_row0 + tt * it.drow, it.bi, pol_once);
       KvCursor<LAYOUT> cur;
-      cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
+      cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last);
       int32_t key0, key_end;
       bool diag;
       int32_t li = 0;  // load index: K_j = 2j, V_j = 2j + 1
       bool ok = true;
       // ACCUMULATE reads the running triple at the end: bring its O tiles and m, l rows
       // into L2 once the K/V pipeline is full, so that they do not delay the first loads.
-      const bool staged = it.q_rows == BM && it.q_row0 + BM <= p.S;
       bool prefetched = (p.mode & CP_MODE_ACCUMULATE) == 0;
       auto prefetch_old = [&]() {
         for (int tt = 0; tt < n_q; ++tt) {
-          const int64_t ml = (int64_t(it.bi) * p.h_q + it.h0 + tt) * p.S + it.q_row0;
-          for (int i = 0; i < it.q_rows; i += 32) {
+          const int32_t row0 = it.q_row0 + tt * it.drow;
+          const int32_t rows = tt ? it.q_rows_b : it.q_rows;
+          const bool staged = rows == BM && row0 + BM <= p.S;
+          const int64_t ml = (int64_t(it.bi) * p.h_q + it.h0 + tt * it.dh) * p.S + row0;
+          for (int i = 0; i < rows; i += 32) {
             prefetch_l2(p.m + ml + i);
             prefetch_l2(p.l + ml + i);
           }
-          prefetch_l2(p.m + ml + it.q_rows - 1);
-          prefetch_l2(p.l + ml + it.q_rows - 1);
+          prefetch_l2(p.m + ml + rows - 1);
+          prefetch_l2(p.l + ml + rows - 1);
           if (staged)
-            for (int c = 0; c < D / 32; ++c) tma_prefetch_4d(&p.tmap_o, c * 32, it.h0 + tt, it.q_row0, it.bi);
+            for (int c = 0; c < D / 32; ++c) tma_prefetch_4d(&p.tmap_o, c * 32, it.h0 + tt * it.dh, row0, it.bi);
         }
         prefetched = true;
       };
@@ -459,8 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     // ------------------------------------------------------------ softmax + epilogue
     const int tt = (warp - 4) / 4;
     const int t = threadIdx.x - 128 * (1 + tt);  // row within the tile == TMEM lane
-    const int h = it.h0 + tt;
-    const int32_t row = it.q_row0 + t;
+    const int h = it.h0 + tt * it.dh;
+    const int32_t row0 = it.q_row0 + tt * it.drow;  // this tile's first row
+    const int32_t rows = tt ? it.q_rows_b : it.q_rows;
+    const int32_t row = row0 + t;
     const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + uint32_t(tt * 128);
     const uint32_t o_addr = tmem + lane_base + K::kOCol + uint32_t(tt * D);
@@ -470,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     bool ok = true;
 
     KvCursor<LAYOUT> cur;
-    cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_row0 + it.q_rows - 1);
+    cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last);
     for (int32_t j = 0; j < n_kv; ++j) {
       int32_t key0 = 0, key_end = 0;
       bool diag = false;
@@ -485,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       float x[BN];
 #pragma unroll
       for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(sr[i]);
-      const bool full = (key0 + BN <= key_end) && (!diag || key0 + BN - 1 <= it.q_row0);
+      const bool full = (key0 + BN <= key_end) && (!diag || key0 + BN - 1 <= row0);
       if (!full) {
 #pragma unroll
         for (int i = 0; i < BN; ++i) {
@@ -566,10 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const float fre = (m_true == -INFINITY) ? 0.f : ex2(m_ref - m_true);
       const float m_new_nat = m_true * kLn2;
       const float l_new = l_run * fre;
-      const bool row_ok = t < it.q_rows && row < p.S;
+      const bool row_ok = t < rows && row < p.S;
       const bool accumulate = (p.mode & CP_MODE_ACCUMULATE) != 0;
       // A whole 128-row tile moves its O rows through shared memory with TMA.
-      const bool staged = it.q_rows == BM && it.q_row0 + BM <= p.S;
+      const bool staged = rows == BM && row0 + BM <= p.S;
       const int64_t ml_off = (int64_t(it.bi) * p.h_q + h) * p.S + row;
       float alpha = 0.f, beta = 1.f, l_out = l_new, m_out = m_new_nat;
       if (accumulate && row_ok) {
@@ -602,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           mbar_expect_tx(bar_l(tt), uint32_t(BM * D * 4));
 #pragma unroll
           for (int c = 0; c < D / 32; ++c)
-            tma_load_4d(stage + uint32_t(c * BM * 128), &p.tmap_o, bar_l(tt), c * 32, h, it.q_row0, it.bi);
+            tma_load_4d(stage + uint32_t(c * BM * 128), &p.tmap_o, bar_l(tt), c * 32, h, row0, it.bi);
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar_l(tt), 0, abort_flag))) {
           ok = false;
@@ -648,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
             const uint64_t pol_once = l2_policy_evict_first();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c)
-              tma_store_4d_hint(&p.tmap_o, stage + uint32_t(c * BM * 128), c * 32, h, it.q_row0, it.bi, pol_once);
+              tma_store_4d_hint(&p.tmap_o, stage + uint32_t(c * BM * 128), c * 32, h, row0, it.bi, pol_once);
             bulk_commit();
             bulk_wait_all();
           }
@@ -799,7 +823,11 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   p.C = int32_t(d.S / (2 * d.cp));
   p.tpc = (p.C + BM - 1) / BM;
   p.group = int32_t(d.h_q / d.h_kv);
-  p.ppg = (p.group + 1) / 2;
+  // Two query tiles share each K/V tile in a CTA: two heads of a kv group (even groups),
+  // or two consecutive row tiles of one head (odd groups, unless a chunk is one tile).
+  p.row_pairs = (p.group % 2 == 1 && (p.group == 1 || p.tpc > 1)) ? 1 : 0;
+  p.ipc = p.row_pairs ? (p.tpc + 1) / 2 : p.tpc;
+  p.ppg = p.row_pairs ? p.group : (p.group + 1) / 2;
   p.n_pairs = int32_t(d.h_kv) * p.ppg;
   p.step_begin = step_begin;
   p.step_end = step_end;
@@ -827,7 +855,7 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
     p.unit_groups = int32_t(groups);
   }
   const int64_t n_items =
-      int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * p.n_pairs;
+      int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.ipc * d.b * p.n_pairs;
   if (n_items > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
   if (layout == CP_LAYOUT_SEQUENTIAL)
     return d.d == 128 ? launch_d<128, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream)

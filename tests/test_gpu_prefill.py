@@ -239,9 +239,11 @@ def test_sequential_layout_step_triples():
                 assert_out_close(go[live] / gl[live][:, None], ro[live] / rl[live][:, None], f"seq t{t} r{r}")
 
 
+@pytest.mark.parametrize("heads", [(4, 2), (3, 3), (6, 2)], ids=["gqa2", "mha", "g3"])
 @pytest.mark.parametrize("layout", [cpa.CP_LAYOUT_BALANCED, SEQ])
-def test_rank_ranges_touch_only_their_rows_and_compose(layout):
-    b, S, hq, hkv, d, cp = 1, 2048, 4, 2, 128, 4
+def test_rank_ranges_touch_only_their_rows_and_compose(layout, heads):
+    b, S, d, cp = 1, 2048, 128, 4
+    hq, hkv = heads
     q, k, v = _inputs(b, S, hq, hkv, d, 0.5, seed=33)
     full = ring_buffers(b, S, hq, d)
     _run_ranks(q, k, v, cp, layout, 0, cp, 0, cp, EMIT | FIN, full)
@@ -285,7 +287,7 @@ def test_bounded_wait_timeout_is_reported_and_recovers():
     assert_out_close(o.cpu().numpy(), ref_out, "after recovery")
 
 
-@pytest.mark.parametrize("name", ["gqa", "long"])
+@pytest.mark.parametrize("name", ["gqa", "long", "mha"])
 def test_full_size_workload_sampled_rows(name):
     """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled."""
     w = synth.WORKLOADS[name]
@@ -404,3 +406,40 @@ def test_per_step_accumulate_chain_at_full_size():
         assert_out_close(chain[0][0, rows, h].cpu().numpy(), ref_out[0], f"chain head {h}")
     del q, k, v, chain, fused
     torch.cuda.empty_cache()
+
+
+# Odd groups (one query head per K/V head, or three): a CTA takes two consecutive 128-row
+# tiles of one head, and the first tile sees one fully masked K/V tile on its chunk's
+# diagonal.  Chunks of 250 rows (a 122-row second tile), 384 rows (a pair and a single
+# tile) and 320 rows (a pair and a 64-row single).
+MHA = [(1, 1000, 2, 2, 128, 2, 1.0), (2, 3072, 2, 2, 128, 4, 0.5), (1, 1280, 3, 3, 64, 2, 1.0),
+       (1, 1536, 6, 2, 128, 2, 0.5), (2, 1000, 3, 1, 64, 2, 1.0)]
+
+
+@pytest.mark.parametrize("case", MHA, ids=["C250", "C384_b2", "C320_d64", "g3_C384", "g3_C250_b2"])
+def test_row_paired_tiles_full_ring_and_steps(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=3 + (hash(case) & 0xFF))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    scale = 1.0 / math.sqrt(d)
+    o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+    ref_out, ref_m, ref_l, _ = OA.full_causal_attention(qf, kf, vf, scale)
+    assert_out_close(o.cpu().numpy(), ref_out, f"out {case}")
+    assert np.abs(m.cpu().numpy() - ref_m).max() <= LSE_ABS
+    # every ring step's triple, and the steps accumulated in reverse order
+    bufs = ring_buffers(b, S, hq, d, identity=True)
+    for t in range(cp):
+        o, m, l = run_ring(q, k, v, cp, t, t + 1, EMIT)
+        o, m, l = o.cpu().numpy(), m.cpu().numpy(), l.cpu().numpy()
+        for r in range(cp):
+            rows, rm, rl, ro = OR.ring_step_triple(qf, kf, vf, scale, cp, r, t)
+            gm, gl = m[:, :, rows], l[:, :, rows]
+            go = np.moveaxis(o[:, rows], 1, 2)
+            empty = np.isneginf(rm)
+            assert np.all(np.isneginf(gm[empty])) and np.all(gl[empty] == 0) and np.all(go[empty] == 0)
+            live = ~empty
+            assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
+            assert_out_close(go[live] / gl[live][:, None], ro[live] / rl[live][:, None], f"step {t} rank {r}")
+    for i, t in enumerate(range(cp - 1, -1, -1)):
+        run_ring(q, k, v, cp, t, t + 1, ACC | (FIN if i == cp - 1 else 0), bufs)
+    assert_out_close(bufs[0].cpu().numpy(), ref_out, "accumulated")
