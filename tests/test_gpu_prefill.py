@@ -6,6 +6,7 @@ a step must be exactly the identity (-inf, 0, 0).
 """
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -41,6 +42,20 @@ def _lib():
     from context_ring_attention_cp_gb300 import _build
     _build.build()
     cpa.load_library()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _paired_tiles():
+    # Launches under one wave of single tiles run one tile per CTA; the small parity cases
+    # here would all take that path.  Force two tiles per CTA (the path of every launch of
+    # more than a wave); test_tile_pairing_modes_give_the_same_bits covers the others.
+    old = os.environ.get("CPATTN_RING_PAIRING")
+    os.environ["CPATTN_RING_PAIRING"] = "pair"
+    yield
+    if old is None:
+        del os.environ["CPATTN_RING_PAIRING"]
+    else:
+        os.environ["CPATTN_RING_PAIRING"] = old
 
 
 def _inputs(b, S, hq, hkv, d, std, seed):
@@ -443,3 +458,23 @@ def test_row_paired_tiles_full_ring_and_steps(case):
     for i, t in enumerate(range(cp - 1, -1, -1)):
         run_ring(q, k, v, cp, t, t + 1, ACC | (FIN if i == cp - 1 else 0), bufs)
     assert_out_close(bufs[0].cpu().numpy(), ref_out, "accumulated")
+
+
+@pytest.mark.parametrize("case", [SMALL[0], SMALL[1], SMALL[2], SMALL[3], MHA[1], MHA[3], (1, 2048, 8, 2, 128, 4, 0.5)],
+                         ids=["tiny", "b2", "C250_g2", "C96_g3", "C384_mha", "g3_C384", "gqa4"])
+def test_tile_pairing_modes_give_the_same_bits(case, monkeypatch):
+    """One tile per CTA, two tiles per CTA and the automatic choice compute every row alike."""
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=11)
+    got = {}
+    for mode in ("single", "pair", "auto"):
+        monkeypatch.setenv("CPATTN_RING_PAIRING", mode)
+        full = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        step = run_ring(q, k, v, cp, cp - 1, cp, EMIT)
+        acc = run_ring(q, k, v, cp, 0, 1, EMIT)
+        run_ring(q, k, v, cp, 1, 2, ACC | FIN, acc)
+        got[mode] = (full, step, acc)
+    for mode in ("pair", "auto"):
+        for xs, ys in zip(got["single"], got[mode]):
+            for x, y in zip(xs, ys):
+                assert torch.equal(x, y), f"{mode} {case}"
