@@ -78,11 +78,6 @@ constexpr int64_t kL2UnitBudget = int64_t(40) << 20;  // K/V bytes of one group 
 
 __device__ int32_t g_ring_status = 0;
 
-// How a CTA's two query tiles are chosen (both share every K/V tile).
-constexpr int32_t kSingleTiles = 0;  // one tile per CTA: more CTAs, for launches under one wave
-constexpr int32_t kHeadPairs = 1;    // two heads of one kv group, same rows
-constexpr int32_t kRowPairs = 2;     // two consecutive row tiles of one head
-
 template <int D>
 struct Cfg {
   static constexpr int kSlab = BM * 128;             // bytes of one 64-column swizzled slab
@@ -108,8 +103,8 @@ struct RingParams {
   int32_t C;          // chunk length S / (2 cp)
   int32_t cp;
   int32_t tpc;        // query tiles per chunk
-  int32_t pair_mode;  // tiles per CTA: kSingleTiles, kHeadPairs or kRowPairs
-  int32_t ipc;        // work items per chunk along its rows: tpc, or ceil(tpc / 2) for row pairs
+  int32_t row_pairs;  // 1: a CTA takes two consecutive query tiles of one head (odd group)
+  int32_t ipc;        // work items per chunk along its rows: tpc, or ceil(tpc / 2) with row_pairs
   int32_t n_pairs;    // head pairs per batch entry
   int32_t ppg;        // head pairs per kv group
   int32_t group;      // h_q / h_kv
@@ -218,7 +213,7 @@ struct KvCursor {
 // One CTA's work: query tile A and, when has_b, tile B, which share every K/V tile.
 // Tile B is the next query head of the kv group (dh = 1, same rows; even groups) or
 // the next 128 rows of the same head (drow = BM; odd groups, so that no head is left
-// without a partner).  Launches of less than a wave of single tiles keep one tile per CTA.
+// without a partner).
 struct Item {
   int32_t bi, h0, has_b, kvh;
   int32_t c_q, r, q_row0, q_rows;
@@ -245,7 +240,7 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t unit = g * upg + u;
   it.bi = unit / int32_t(p.h_kv);
   it.kvh = unit - it.bi * int32_t(p.h_kv);
-  it.h0 = it.kvh * p.group + (p.pair_mode == kHeadPairs ? 2 * i : i);
+  it.h0 = it.kvh * p.group + (p.row_pairs ? i : 2 * i);
   // a-th selected chunk in ascending order.  Balanced: the ranks' head chunks
   // [rank_begin, rank_end) then their tail chunks [2cp-rank_end, 2cp-rank_begin);
   // sequential: chunks [2 rank_begin, 2 rank_end).  With one chunk per rank selected,
@@ -261,10 +256,10 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
     it.c_q = (a < nr) ? p.rank_begin + a : 2 * p.cp - p.rank_end + (a - nr);
     it.r = (it.c_q < p.cp) ? it.c_q : 2 * p.cp - 1 - it.c_q;
   }
-  const int32_t tile0 = p.pair_mode == kRowPairs ? 2 * kq : kq;  // the item's first query tile in its chunk
+  const int32_t tile0 = p.row_pairs ? 2 * kq : kq;  // first query tile of the item in its chunk
   it.q_row0 = it.c_q * p.C + BM * tile0;
   it.q_rows = min(BM, p.C - BM * tile0);
-  if (p.pair_mode == kRowPairs) {
+  if (p.row_pairs) {
     it.dh = 0;
     it.drow = BM;
     it.q_rows_b = max(0, min(BM, p.C - BM * (tile0 + 1)));
@@ -274,7 +269,7 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
     it.dh = 1;
     it.drow = 0;
     it.q_rows_b = it.q_rows;
-    it.has_b = (p.pair_mode == kHeadPairs && 2 * i + 1 < p.group) ? 1 : 0;
+    it.has_b = (2 * i + 1 < p.group) ? 1 : 0;
     it.q_last = it.q_row0 + it.q_rows - 1;
   }
   return it;
@@ -847,17 +842,20 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   p.group = int32_t(d.h_q / d.h_kv);
   // Two query tiles share each K/V tile in a CTA: two heads of a kv group (even groups),
   // or two consecutive row tiles of one head (odd groups, unless a chunk is one tile).
-  // A launch whose single tiles fit in one wave keeps one tile per CTA: pairing would
-  // halve its CTAs and lengthen each CTA's chain (a tiny prefill: 17 against 21 us).
+  bool row_pairs = p.group % 2 == 1 && (p.group == 1 || p.tpc > 1);
+  // With one query head per kv head, a launch whose single tiles fit in one wave runs one
+  // tile per CTA (the head-pair form, which finds no second head): pairing would halve its
+  // CTAs and lengthen each CTA's chain (a tiny prefill: 15.5 against 19.4 us).
   // CPATTN_RING_PAIRING=single|pair overrides the choice; the results are the same bits.
-  const int64_t n_single =
-      int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * d.h_q;
-  int32_t pairing = (p.group % 2 == 0 || (p.group > 1 && p.tpc == 1)) ? kHeadPairs : kRowPairs;
-  const int32_t forced = ring_pairing_override();
-  if (forced == 0 || (forced < 0 && n_single <= int64_t(sm_count()))) pairing = kSingleTiles;
-  p.pair_mode = pairing;
-  p.ipc = pairing == kRowPairs ? (p.tpc + 1) / 2 : p.tpc;
-  p.ppg = pairing == kHeadPairs ? (p.group + 1) / 2 : p.group;
+  if (p.group == 1) {
+    const int64_t n_single =
+        int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * d.h_q;
+    const int32_t forced = ring_pairing_override();
+    if (forced == 0 || (forced < 0 && n_single <= int64_t(sm_count()))) row_pairs = false;
+  }
+  p.row_pairs = row_pairs ? 1 : 0;
+  p.ipc = p.row_pairs ? (p.tpc + 1) / 2 : p.tpc;
+  p.ppg = p.row_pairs ? p.group : (p.group + 1) / 2;
   p.n_pairs = int32_t(d.h_kv) * p.ppg;
   p.step_begin = step_begin;
   p.step_end = step_end;

@@ -126,9 +126,9 @@ CPATTN_API cp_status cp_plan_chunks(int64_t S, int32_t cp, int32_t layout, int64
  * q, k, v: bf16 device, layouts above; o, m, l: fp32 device, layouts above.
  * Tiling: each CTA computes two 128-row query tiles that share every K/V tile: two
  * heads of one kv group (even h_q / h_kv) or two consecutive row tiles of one head
- * (odd).  A launch with at most one wave (SM count) of single tiles keeps one tile per
- * CTA.  The environment variable CPATTN_RING_PAIRING=single|pair overrides that choice
- * at each call; every choice gives the same bits.
+ * (odd).  With h_q == h_kv, a launch with at most one wave (SM count) of single tiles
+ * keeps one tile per CTA; the environment variable CPATTN_RING_PAIRING=single|pair
+ * overrides that choice at each call, and every choice gives the same bits.
  * Supported: d in {64, 128}; causal = 1; every pointer 16-byte aligned.
  * Errors: cp < 1, S % (2cp) != 0, h_q % h_kv != 0, any size < 1, scale <= 0 or
  * not finite, 0 <= step_begin < step_end <= cp violated, unknown mode bits, NULL or
