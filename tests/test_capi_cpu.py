@@ -187,6 +187,8 @@ def _desc(cpa, **kw):
     (dict(cp=0), 1), (dict(cp=-1), 1), (dict(S=1000, cp=8), 1), (dict(S=0), 1), (dict(b=0), 1),
     (dict(h_q=6, h_kv=4), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1),
     (dict(scale=float("nan")), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(causal=0), 2),
+    # beyond the kernel's 32-bit row, batch and head indexing
+    (dict(S=1 << 30, cp=1), 2), (dict(b=65536, S=2, cp=1), 2), (dict(h_q=65536, h_kv=65536, S=2, cp=1), 2),
 ])
 def test_ring_rejects_descriptors(cpa, kw, status):
     with pytest.raises(cpa.CpError) as e:
