@@ -17,6 +17,27 @@
 
 using namespace cpattn;
 
+cudaError_t cpattn::current_sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 cpattn::tensor_map_encoder() {
+  // A function-local static is initialised once, even under concurrent first calls.
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) !=
+            cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
 namespace {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -46,13 +67,6 @@ cp_status check_decode_desc(const cp_attn_desc* d) {
   if (d->causal != 0) return CP_ERR_UNSUPPORTED;
   if (!decode_supported(*d)) return CP_ERR_UNSUPPORTED;
   return CP_OK;
-}
-
-cudaError_t current_sm_count(int* sms) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
 }
 
 // ---------------------------------------------------------------------------

@@ -2,12 +2,20 @@
 // Every function here is called only after capi.cpp has validated its arguments.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/cpattn.h"
 
 namespace cpattn {
+
+// ---- host helpers shared by the kernel files (capi.cpp) ----------------------
+// The driver's cuTensorMapEncodeTiled, looked up once per process; null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// SM count of the calling thread's current device.
+cudaError_t current_sm_count(int* sms);
 
 // ---- LSE merge (merge.cu) --------------------------------------------------
 struct MergeParams {

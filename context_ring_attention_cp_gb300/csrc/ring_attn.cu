@@ -746,24 +746,10 @@ __global__ void ring_wait_timeout_selftest_kernel() {
   __syncthreads();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult qres;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) !=
-            cudaSuccess ||
-        qres != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // 4-D bf16 map over a [b, S, h, d] tensor: dims (d, h, S, b), box (64, 1, 128, 1), 128-byte swizzle.
 // 4-D fp32 map over the [b, S, h, d] output: box (32, 1, 128, 1), 128-byte swizzle.
 bool encode_map_o(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_t h, int64_t d) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(h), cuuint64_t(S), cuuint64_t(b)};
   const cuuint64_t strides[3] = {cuuint64_t(d * 4), cuuint64_t(h * d * 4), cuuint64_t(S * h * d * 4)};
@@ -776,7 +762,7 @@ bool encode_map_o(CUtensorMap* map, const void* base, int64_t b, int64_t S, int6
 }
 
 bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_t h, int64_t d) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(h), cuuint64_t(S), cuuint64_t(b)};
   const cuuint64_t strides[3] = {cuuint64_t(d * 2), cuuint64_t(h * d * 2), cuuint64_t(S * h * d * 2)};
@@ -795,13 +781,6 @@ int32_t ring_pairing_override() {
   if (strcmp(e, "single") == 0) return 0;
   if (strcmp(e, "pair") == 0) return 1;
   return -1;
-}
-
-int32_t sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 1;
-  return n;
 }
 
 template <int D, int LAYOUT>
@@ -851,7 +830,9 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
     const int64_t n_single =
         int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * d.h_q;
     const int32_t forced = ring_pairing_override();
-    if (forced == 0 || (forced < 0 && n_single <= int64_t(sm_count()))) row_pairs = false;
+    int sms = 0;
+    if (forced < 0 && current_sm_count(&sms) != cudaSuccess) return CP_ERR_CUDA;
+    if (forced == 0 || (forced < 0 && n_single <= int64_t(sms))) row_pairs = false;
   }
   p.row_pairs = row_pairs ? 1 : 0;
   p.ipc = p.row_pairs ? (p.tpc + 1) / 2 : p.tpc;
