@@ -74,7 +74,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "1e4ed6ef04870a34", "bytes": 891654400}
+RING_TRAFFIC = {"sha256_prefix": "b5ba9c34b938a731", "bytes": 892353536}
 
 
 def ring_traffic():
