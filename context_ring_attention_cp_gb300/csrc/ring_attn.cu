@@ -105,8 +105,8 @@ struct RingParams {
   int32_t tpc;        // query tiles per chunk
   int32_t row_pairs;  // 1: a CTA takes two consecutive query tiles of one head (odd group)
   int32_t ipc;        // work items per chunk along its rows: tpc, or ceil(tpc / 2) with row_pairs
-  int32_t n_pairs;    // head pairs per batch entry
-  int32_t ppg;        // head pairs per kv group
+  int32_t n_pairs;    // items per batch entry and row item: h_kv * ppg
+  int32_t ppg;        // items per kv group and row item: head pairs, or heads with row_pairs
   int32_t group;      // h_q / h_kv
   int32_t step_begin, step_end;
   int32_t mode;
@@ -226,7 +226,7 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t nr = p.rank_end - p.rank_begin;
   const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.ipc;  // row items of the selected chunks
   // Units (sequence, kv head) in groups whose K/V fits in L2; within a group, the
-  // latest chunk (most keys) first, then the group's head pairs.
+  // latest chunk (most keys) first, then the group's head pairs (or heads).
   // The launch has fewer than 2^31 items, so every index here fits 32 bits.
   const int32_t upg = int32_t(p.b * p.h_kv) / p.unit_groups;  // units per group
   const int32_t per_tile = upg * p.ppg;
