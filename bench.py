@@ -74,7 +74,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture summarised in
 # profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
 # the source that was captured (sha256 prefix below); otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "b5ba9c34b938a731", "bytes": 892353536}
+RING_TRAFFIC = {"sha256_prefix": "c9d394c7b0694ff1", "bytes": 893814272}
 
 
 def ring_traffic():
