@@ -302,12 +302,19 @@ def test_bounded_wait_timeout_is_reported_and_recovers():
     assert_out_close(o.cpu().numpy(), ref_out, "after recovery")
 
 
-@pytest.mark.parametrize("name", ["gqa", "long", "mha"])
+@pytest.mark.parametrize("name", ["gqa", "long", "mha", "gqa-sequential"])
 def test_full_size_workload_sampled_rows(name):
-    """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled."""
-    w = synth.WORKLOADS[name]
+    """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled.
+    gqa-sequential: the GQA workload under the sequential chunk layout, one launch per
+    virtual rank as the rank-balance measurement runs it."""
+    w = synth.WORKLOADS[name.split("-")[0]]
     q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
-    o, m, l = run_ring(q, k, v, w["cp"], 0, w["cp"], EMIT | FIN)
+    if name.endswith("sequential"):
+        o, m, l = ring_buffers(w["b"], w["S"], w["h_q"], w["d"])
+        for r in range(w["cp"]):
+            _run_ranks(q, k, v, w["cp"], SEQ, r, r + 1, 0, w["cp"], EMIT | FIN, (o, m, l))
+    else:
+        o, m, l = run_ring(q, k, v, w["cp"], 0, w["cp"], EMIT | FIN)
     rows = synth.sample_rows(w["S"], w["cp"], 64, seed=w["seed"])
     heads = [0, 5, w["h_q"] - 1]
     g = w["h_q"] // w["h_kv"]
