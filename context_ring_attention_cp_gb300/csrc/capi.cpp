@@ -559,9 +559,11 @@ cp_status cp_selftest_wait_timeout(void* cuda_stream) {
 cp_status cp_take_device_status(void* cuda_stream, int32_t* status) {
   if (status == nullptr) return CP_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return CP_ERR_CUDA;
-  int32_t s = CP_OK, s2 = CP_OK;
-  if (ring_take_status(&s) != cudaSuccess || mqa_take_status(&s2) != cudaSuccess) return CP_ERR_CUDA;
-  *status = (s != CP_OK) ? s : s2;
+  int32_t s = CP_OK, s2 = CP_OK, s3 = CP_OK;
+  if (ring_take_status(&s) != cudaSuccess || mqa_take_status(&s2) != cudaSuccess ||
+      merge_take_status(&s3) != cudaSuccess)
+    return CP_ERR_CUDA;
+  *status = (s != CP_OK) ? s : (s2 != CP_OK ? s2 : s3);
   return CP_OK;
 }
 

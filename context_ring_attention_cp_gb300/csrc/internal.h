@@ -33,6 +33,8 @@ struct MergeParams {
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 // The halving tree over n_parts = 2^k parts (k in 1..8) in one pass; order[] is not used.
 cudaError_t launch_merge_tree(const MergeParams& p, cudaStream_t stream);
+// Reads and clears the merge kernels' device status word (after the caller synchronised).
+cudaError_t merge_take_status(int32_t* status);
 
 // ---- pass-Q decode partials (decode.cu) ------------------------------------
 // Key ranges per shard chosen for the device's SM count; n_parts = cp * splits.

@@ -12,13 +12,18 @@
 // stages the 2 x n_parts x kRowsPerCta scalars (m, l) with coalesced loads into shared
 // memory, then each warp streams the O rows of its rows part by part, lanes
 // owning float4 slices of d, with eight (d <= 128) down to two (d = 512) parts of loads
-// in flight per lane.
+// in flight per lane.  For d = 128 and up to 64 parts, one thread per CTA instead
+// streams every part's block of O rows into a ring of shared-memory slots with TMA, and
+// the warps fold the same parts in the same order (the same bits).
 
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "internal.h"
+#include "tc_ptx.h"
 
 namespace cpattn {
 namespace {
@@ -141,6 +146,170 @@ __global__ void __launch_bounds__(kThreads, NCH == 1 ? 5 : 1) lse_merge_kernel(c
       if (p.l_out) p.l_out[off] = lsum;
     }
   }
+}
+
+// d = 128, up to 64 parts: the same fold fed by TMA.  The kernel above keeps at
+// most eight parts of loads in flight per warp and drains between batches (82 % of
+// DRAM peak on the merge stress).  Here one thread streams each part's block of
+// kRowsPerCta x 128 O values into a ring of shared-memory slots, kTmaSlots parts
+// ahead of the slowest warp; each warp folds two rows from shared memory with the
+// same arithmetic in the same order, so the result is the same bits.
+constexpr int kTmaD = 128;
+constexpr int kTmaSlots = 6;  // 4 CTAs per SM; 4 slots (5 CTAs) measured the same, 12 (2 CTAs) 10 % slower
+constexpr uint32_t kTmaSlotBytes = kRowsPerCta * kTmaD * 4;  // 8 KB
+constexpr int kTmaMaxParts = 64;  // m and l staging stays at most 8 KB (58 KB of shared memory a CTA)
+constexpr int kTmaRowsPerWarp = kRowsPerCta / kWarps;
+
+__device__ int32_t g_merge_status = 0;
+
+struct MergeTmaParams {
+  CUtensorMap map_o;  // o_parts as fp32 (d, heads, rows, n_parts * batch), box (128, 1, kRowsPerCta, 1)
+  MergeParams p;
+};
+
+size_t merge_tma_smem_bytes(int32_t n_parts) {
+  return 1024 + size_t(kTmaSlots) * kTmaSlotBytes + size_t(2) * n_parts * kRowsPerCta * 4 +
+         size_t(2) * kTmaSlots * 8 + 16;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) lse_merge_tma_kernel(const __grid_constant__ MergeTmaParams tp) {
+  using namespace tc;
+  const MergeParams& p = tp.p;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int n_parts = p.n_parts;
+  const uint32_t ring = smem_u32(base);
+  float* sm_m = reinterpret_cast<float*>(base + kTmaSlots * kTmaSlotBytes);  // [n_parts][kRowsPerCta]
+  float* sm_l = sm_m + n_parts * kRowsPerCta;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm_l + n_parts * kRowsPerCta);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(bars + 2 * kTmaSlots);
+  auto full = [&](int sl) { return smem_u32(&bars[sl]); };
+  auto empty = [&](int sl) { return smem_u32(&bars[kTmaSlots + sl]); };
+
+  const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t tile = blockIdx.x;
+  const int64_t rb = tile % row_blocks;
+  const int64_t bh = tile / row_blocks;
+  const int64_t h = bh % p.heads;
+  const int64_t bi = bh / p.heads;
+  const int64_t row0 = rb * kRowsPerCta;
+
+  // Part kpos (fold order) into slot kpos % kTmaSlots.
+  auto issue = [&](int kpos) {
+    const int sl = kpos % kTmaSlots;
+    mbar_expect_tx(full(sl), kTmaSlotBytes);
+    tma_load_4d(ring + sl * kTmaSlotBytes, &tp.map_o, full(sl), 0, int32_t(h), int32_t(row0),
+                int32_t(int64_t(p.order[kpos]) * p.batch + bi));
+  };
+  // The first parts stream in while the m and l scalars are staged.
+  if (threadIdx.x == 0) {
+    for (int sl = 0; sl < kTmaSlots; ++sl) {
+      mbar_init(full(sl), 1);
+      mbar_init(empty(sl), kWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int kpos = 0; kpos < n_parts && kpos < kTmaSlots; ++kpos) issue(kpos);
+  }
+  for (int idx = threadIdx.x; idx < n_parts * kRowsPerCta; idx += kThreads) {
+    const int kpos = idx / kRowsPerCta;
+    const int r = idx % kRowsPerCta;
+    const int part = p.order[kpos];
+    const int64_t row = row0 + r;
+    float mv = -INFINITY, lv = 0.f;
+    if (row < p.rows) {
+      const int64_t off = ((int64_t(part) * p.batch + bi) * p.heads + h) * p.rows + row;
+      mv = p.m_parts[off];
+      lv = p.l_parts[off];
+    }
+    sm_m[idx] = mv;
+    sm_l[idx] = lv;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  float shift[kTmaRowsPerWarp], mxr[kTmaRowsPerWarp], lsum[kTmaRowsPerWarp];
+  float4 acc[kTmaRowsPerWarp];
+#pragma unroll
+  for (int rr = 0; rr < kTmaRowsPerWarp; ++rr) {
+    const int r = warp * kTmaRowsPerWarp + rr;
+    float mx = -INFINITY;
+    for (int kpos = lane; kpos < n_parts; kpos += 32) mx = fmaxf(mx, sm_m[kpos * kRowsPerCta + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    mxr[rr] = mx;
+    shift[rr] = (mx == -INFINITY) ? 0.f : mx;
+    lsum[rr] = 0.f;
+    acc[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  bool ok = true;
+  for (int kpos = 0; kpos < n_parts; ++kpos) {
+    const int sl = kpos % kTmaSlots;
+    const uint32_t ph = uint32_t((kpos / kTmaSlots) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(sl), ph, abort_flag, &g_merge_status))) {
+      ok = false;
+      break;
+    }
+#pragma unroll
+    for (int rr = 0; rr < kTmaRowsPerWarp; ++rr) {
+      const int r = warp * kTmaRowsPerWarp + rr;
+      const float w = expf(sm_m[kpos * kRowsPerCta + r] - shift[rr]);
+      lsum[rr] = fmaf(w, sm_l[kpos * kRowsPerCta + r], lsum[rr]);
+      const float4 x = ld_shared_v4(ring + sl * kTmaSlotBytes + uint32_t((r * kTmaD + lane * 4) * 4));
+      acc[rr].x = fmaf(w, x.x, acc[rr].x);
+      acc[rr].y = fmaf(w, x.y, acc[rr].y);
+      acc[rr].z = fmaf(w, x.z, acc[rr].z);
+      acc[rr].w = fmaf(w, x.w, acc[rr].w);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(sl));
+    // The slot is refilled once every warp has read it.
+    if (threadIdx.x == 0 && kpos + kTmaSlots < n_parts) {
+      if (!mbar_wait_bounded(empty(sl), ph, abort_flag, &g_merge_status)) {
+        ok = false;
+      } else {
+        issue(kpos + kTmaSlots);
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) break;
+  }
+  if (!ok || *abort_flag) {
+    // Thread 0 issued every copy: it stays until those in flight have landed, which
+    // keeps the CTA's shared memory allocated; the other threads leave at once.
+    if (threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 50000ull) {
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int rr = 0; rr < kTmaRowsPerWarp; ++rr) {
+    const int r = warp * kTmaRowsPerWarp + rr;
+    const int64_t row = row0 + r;
+    if (row >= p.rows) break;
+    const float ls = lsum[rr];
+    const float inv = (p.finalize && ls > 0.f) ? 1.f / ls : 1.f;
+    const bool zero = p.finalize && !(ls > 0.f);
+    float4 y = acc[rr];
+    if (zero) {
+      y = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (p.finalize) {
+      y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
+    }
+    reinterpret_cast<float4*>(p.o_out + ((bi * p.rows + row) * p.heads + h) * kTmaD)[lane] = y;
+    if (lane == 0) {
+      const int64_t off = (bi * p.heads + h) * p.rows + row;
+      if (p.m_out) p.m_out[off] = mxr[rr];
+      if (p.l_out) p.l_out[off] = ls;
+    }
+  }
+}
+
+bool merge_tma_enabled() {
+  const char* e = getenv("CPATTN_MERGE_TMA");
+  return e == nullptr || strcmp(e, "0") != 0;
 }
 
 // rows == 1 (the decode reduce: one triple per sequence and head).  One CTA per
@@ -494,6 +663,28 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t row_blocks = (p.rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t tiles = row_blocks * p.batch * p.heads;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (p.d == kTmaD && p.n_parts <= kTmaMaxParts && p.rows < (int64_t(1) << 31) && p.heads < (int64_t(1) << 31) &&
+      int64_t(p.n_parts) * p.batch < (int64_t(1) << 31) && enc != nullptr && merge_tma_enabled()) {
+    MergeTmaParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.p = p;
+    const cuuint64_t dims[4] = {cuuint64_t(kTmaD), cuuint64_t(p.heads), cuuint64_t(p.rows),
+                                cuuint64_t(int64_t(p.n_parts) * p.batch)};
+    const cuuint64_t strides[3] = {cuuint64_t(kTmaD * 4), cuuint64_t(p.heads * kTmaD * 4),
+                                   cuuint64_t(p.rows * p.heads * kTmaD * 4)};
+    const cuuint32_t box[4] = {kTmaD, 1, kRowsPerCta, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(&tp.map_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(p.o_parts), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const size_t tsmem = merge_tma_smem_bytes(p.n_parts);
+    cudaError_t e = cudaFuncSetAttribute(lse_merge_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tsmem));
+    if (e != cudaSuccess) return e;
+    lse_merge_tma_kernel<<<unsigned(tiles), kThreads, tsmem, stream>>>(tp);
+    return cudaGetLastError();
+  }
   const size_t smem = size_t(2) * p.n_parts * kRowsPerCta * sizeof(float);
   const int nch = int((p.d / 4 + 31) / 32);
   cudaError_t e = cudaSuccess;
@@ -514,6 +705,16 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+cudaError_t merge_take_status(int32_t* status) {
+  int32_t s = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&s, g_merge_status, sizeof(s));
+  if (e != cudaSuccess) return e;
+  const int32_t zero = 0;
+  e = cudaMemcpyToSymbol(g_merge_status, &zero, sizeof(zero));
+  *status = s;
+  return e;
 }
 
 }  // namespace cpattn

@@ -341,3 +341,27 @@ def test_decode_scale_is_the_one_passed(case):
     ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), scale)
     assert_out_close(out.cpu().numpy(), ref_out, f"decode scale {case}")
     assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("shape", [(2, 1, 37, 3, 128), (8, 2, 300, 5, 128), (32, 1, 96, 4, 128),
+                                   (64, 3, 17, 2, 128), (13, 1, 16, 1, 128)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("finalize", [False, True])
+def test_tma_merge_gives_the_register_merges_bits(shape, finalize, monkeypatch):
+    """d = 128 and up to 64 parts take the TMA-fed merge; it folds the same parts in the same
+    order with the same arithmetic as the register-pipelined merge (CPATTN_MERGE_TMA=0)."""
+    n, b, rows, heads, d = shape
+    gen = torch.Generator(device="cpu").manual_seed(1000 + n + rows)
+    o = torch.randn((n, b, rows, heads, d), generator=gen).cuda()
+    m = (torch.randn((n, b, heads, rows), generator=gen) * 20).cuda()
+    m[0, 0, 0, :3] = -math.inf  # some identity parts
+    l = torch.rand((n, b, heads, rows), generator=gen).add_(0.5).cuda()
+    l[0, 0, 0, :3] = 0.0
+    order = list(np.random.default_rng(n).permutation(n))
+    got = {}
+    for tma in ("1", "0"):
+        monkeypatch.setenv("CPATTN_MERGE_TMA", tma)
+        got[tma] = _merge(o, m, l, order=order, finalize=finalize)
+        assert cpa.cp_take_device_status() == 0
+    for x, y in zip(got["1"], got["0"]):
+        assert torch.equal(x, y)
