@@ -664,7 +664,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t tiles = row_blocks * p.batch * p.heads;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (p.d == kTmaD && p.n_parts <= kTmaMaxParts && p.rows < (int64_t(1) << 31) && p.heads < (int64_t(1) << 31) &&
+  // TMA coordinates are 32-bit and its strides below 2^40 bytes (rows * heads * 512 B).
+  if (p.d == kTmaD && p.n_parts <= kTmaMaxParts && p.rows * p.heads < (int64_t(1) << 31) &&
       int64_t(p.n_parts) * p.batch < (int64_t(1) << 31) && enc != nullptr && merge_tma_enabled()) {
     MergeTmaParams tp;
     memset(&tp, 0, sizeof(tp));

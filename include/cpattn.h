@@ -199,9 +199,12 @@ CPATTN_API cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_h
  * 0..n_parts-1; NULL = index order).  Parts with m_p = -inf weigh 0; a row whose
  * parts are all the identity stays the identity.  finalize != 0 writes O / l
  * (0 where l = 0) into o_out instead of O.  Outputs must not alias inputs.
+ * With d = 128 and at most 64 parts the O rows are streamed by TMA; the environment
+ * variable CPATTN_MERGE_TMA=0 selects the plain-load kernel, which gives the same bits.
+ * A device-side wait that gives up records CP_ERR_TIMEOUT for cp_take_device_status.
  * Errors: any size < 1, n_parts > CP_MAX_MERGE_PARTS, d % 4 != 0, `order` not a
  * permutation, NULL or misaligned device pointer -> CP_ERR_INVALID_ARGUMENT;
- * d > 512 -> CP_ERR_UNSUPPORTED.
+ * d > 512 -> CP_ERR_UNSUPPORTED; a failed tensor-map encode or launch -> CP_ERR_CUDA.
  */
 CPATTN_API cp_status cp_merge_partials(int64_t batch, int64_t rows, int64_t heads, int64_t d,
                             int32_t n_parts, const float* o_parts, const float* m_parts,
