@@ -125,6 +125,59 @@ def _ptr(x) -> Optional[int]:
     return x.data_ptr()
 
 
+def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, cuda: bool = True) -> Optional[int]:
+    """Address of a tensor argument, after the checks the C ABI cannot make through a plain
+    pointer: dtype, contiguity, size against the descriptor, and device.  A wrong buffer
+    would otherwise be read or written out of bounds by the kernels.  None and raw int
+    addresses pass through unchecked."""
+    if x is None or isinstance(x, int):
+        return x
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{where}: {name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{where}: {name} must be contiguous")
+    if x.numel() < numel:
+        raise ValueError(f"{where}: {name} holds {x.numel()} elements, the descriptor needs {numel}")
+    if x.numel() * x.element_size() < nbytes:
+        raise ValueError(f"{where}: {name} holds {x.numel() * x.element_size()} bytes, {nbytes} were passed")
+    if bool(x.is_cuda) != cuda:
+        raise ValueError(f"{where}: {name} must be a {'CUDA' if cuda else 'host (CPU)'} tensor")
+    return x.data_ptr()
+
+
+def _ring_args(desc, q, k, v, o, m, l, where: str, cuda: bool = True):
+    import torch
+    b, S, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
+    return (_arg(q, "q", where, torch.bfloat16, b * S * hq * d, cuda=cuda),
+            _arg(k, "k", where, torch.bfloat16, b * S * hkv * d, cuda=cuda),
+            _arg(v, "v", where, torch.bfloat16, b * S * hkv * d, cuda=cuda),
+            _arg(o, "o", where, torch.float32, b * S * hq * d, cuda=cuda),
+            _arg(m, "m", where, torch.float32, b * hq * S, cuda=cuda),
+            _arg(l, "l", where, torch.float32, b * hq * S, cuda=cuda))
+
+
+def _merge_args(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out, where: str):
+    import torch
+    n, b, r, h, d = int(n_parts), int(batch), int(rows), int(heads), int(d)
+    return (_arg(o_parts, "o_parts", where, torch.float32, n * b * r * h * d),
+            _arg(m_parts, "m_parts", where, torch.float32, n * b * h * r),
+            _arg(l_parts, "l_parts", where, torch.float32, n * b * h * r),
+            _arg(o_out, "o_out", where, torch.float32, b * r * h * d),
+            _arg(m_out, "m_out", where, torch.float32, b * h * r),
+            _arg(l_out, "l_out", where, torch.float32, b * h * r))
+
+
+def _decode_args(desc, q, k, v, out, m_out, l_out, where: str):
+    import torch
+    b, L, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
+    return (_arg(q, "q", where, torch.bfloat16, b * hq * d),
+            _arg(k, "k", where, torch.bfloat16, b * L * hkv * d),
+            _arg(v, "v", where, torch.bfloat16, b * L * hkv * d),
+            _arg(out, "out", where, torch.float32, b * hq * d),
+            _arg(m_out, "m_out", where, torch.float32, b * hq),
+            _arg(l_out, "l_out", where, torch.float32, b * hq))
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -188,8 +241,9 @@ def cp_ring_step_partial_attn(desc: AttnDesc, step_begin: int, step_end: int, q,
                               mode: int = CP_MODE_EMIT, stream=None) -> None:
     """Ring steps [step_begin, step_end) for all virtual ranks (see include/cpattn.h)."""
     lib = load_library()
-    st = lib.cp_ring_step_partial_attn(ctypes.byref(desc), int(step_begin), int(step_end), _ptr(q), _ptr(k),
-                                       _ptr(v), _ptr(o), _ptr(m), _ptr(l), int(mode), _stream(stream))
+    ptrs = _ring_args(desc, q, k, v, o, m, l, "cp_ring_step_partial_attn")
+    st = lib.cp_ring_step_partial_attn(ctypes.byref(desc), int(step_begin), int(step_end), *ptrs, int(mode),
+                                       _stream(stream))
     _check(st, "cp_ring_step_partial_attn")
 
 
@@ -198,8 +252,9 @@ def cp_ring_rank_partial_attn(desc: AttnDesc, layout: int, rank_begin: int, rank
     """Ring steps [step_begin, step_end) for the virtual ranks [rank_begin, rank_end) under a layout."""
     lib = load_library()
     st = lib.cp_ring_rank_partial_attn(ctypes.byref(desc), int(layout), int(rank_begin), int(rank_end),
-                                       int(step_begin), int(step_end), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m),
-                                       _ptr(l), int(mode), _stream(stream))
+                                       int(step_begin), int(step_end),
+                                       *_ring_args(desc, q, k, v, o, m, l, "cp_ring_rank_partial_attn"), int(mode),
+                                       _stream(stream))
     _check(st, "cp_ring_rank_partial_attn")
 
 
@@ -219,8 +274,10 @@ def cp_ring_attn_host(desc: AttnDesc, q_host, k_host, v_host, o_host, m_host, l_
     least cp_ring_attn_host_workspace_bytes(desc) bytes.  Asynchronous on ``stream``.
     """
     lib = load_library()
-    st = lib.cp_ring_attn_host(ctypes.byref(desc), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host),
-                               _ptr(m_host), _ptr(l_host), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    where = "cp_ring_attn_host"
+    ptrs = _ring_args(desc, q_host, k_host, v_host, o_host, m_host, l_host, where, cuda=False)
+    ws = _arg(workspace, "workspace", where, nbytes=int(workspace_bytes))
+    st = lib.cp_ring_attn_host(ctypes.byref(desc), *ptrs, ws, int(workspace_bytes), _stream(stream))
     _check(st, "cp_ring_attn_host")
 
 
@@ -235,9 +292,10 @@ def cp_merge_partials(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts,
         if order_arr.size != int(n_parts):
             raise CpError(CP_ERR_INVALID_ARGUMENT, "cp_merge_partials")
         order_ptr = order_arr.ctypes.data
-    st = lib.cp_merge_partials(int(batch), int(rows), int(heads), int(d), int(n_parts), _ptr(o_parts),
-                               _ptr(m_parts), _ptr(l_parts), order_ptr, _ptr(o_out), _ptr(m_out), _ptr(l_out),
-                               int(bool(finalize)), _stream(stream))
+    po, pm, pl, oo, om, ol = _merge_args(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out,
+                                         l_out, "cp_merge_partials")
+    st = lib.cp_merge_partials(int(batch), int(rows), int(heads), int(d), int(n_parts), po, pm, pl, order_ptr, oo, om,
+                               ol, int(bool(finalize)), _stream(stream))
     _check(st, "cp_merge_partials")
 
 
@@ -253,9 +311,12 @@ def cp_merge_partials_tree(batch, rows, heads, d, n_parts, o_parts, m_parts, l_p
                            o_out, m_out, l_out, finalize=False, stream=None) -> None:
     """Log-depth tree reduction of n_parts (a power of two) triples; part i merges with part i + n/2."""
     lib = load_library()
-    st = lib.cp_merge_partials_tree(int(batch), int(rows), int(heads), int(d), int(n_parts), _ptr(o_parts),
-                                    _ptr(m_parts), _ptr(l_parts), _ptr(workspace), int(workspace_bytes), _ptr(o_out),
-                                    _ptr(m_out), _ptr(l_out), int(bool(finalize)), _stream(stream))
+    where = "cp_merge_partials_tree"
+    po, pm, pl, oo, om, ol = _merge_args(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out,
+                                         l_out, where)
+    ws = _arg(workspace, "workspace", where, nbytes=int(workspace_bytes))
+    st = lib.cp_merge_partials_tree(int(batch), int(rows), int(heads), int(d), int(n_parts), po, pm, pl, ws,
+                                    int(workspace_bytes), oo, om, ol, int(bool(finalize)), _stream(stream))
     _check(st, "cp_merge_partials_tree")
 
 
@@ -270,8 +331,9 @@ def cp_passq_decode(desc: AttnDesc, q, k, v, workspace, workspace_bytes: int, ou
                     stream=None) -> None:
     """Pass-Q decode: partials over cp shards, then the LSE reduce into ``out``."""
     lib = load_library()
-    st = lib.cp_passq_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(workspace),
-                             int(workspace_bytes), _ptr(out), _ptr(m_out), _ptr(l_out), _stream(stream))
+    pq, pk, pv, po, pm, pl = _decode_args(desc, q, k, v, out, m_out, l_out, "cp_passq_decode")
+    ws = _arg(workspace, "workspace", "cp_passq_decode", nbytes=int(workspace_bytes))
+    st = lib.cp_passq_decode(ctypes.byref(desc), pq, pk, pv, ws, int(workspace_bytes), po, pm, pl, _stream(stream))
     _check(st, "cp_passq_decode")
 
 
@@ -284,8 +346,9 @@ def cp_passq_decode_noalloc(desc: AttnDesc, q, k, v, out, m_out=None, l_out=None
     CP_ERR_UNSUPPORTED before anything is launched.
     """
     lib = load_library()
-    st = lib.cp_passq_decode_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(m_out),
-                                     _ptr(l_out), _stream(stream))
+    st = lib.cp_passq_decode_noalloc(ctypes.byref(desc),
+                                     *_decode_args(desc, q, k, v, out, m_out, l_out, "cp_passq_decode_noalloc"),
+                                     _stream(stream))
     if st == CP_ERR_UNSUPPORTED:
         raise CpError(st, "cp_passq_decode_noalloc (unsupported shape, or partials larger than the "
                           f"{CP_PASSQ_NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)")

@@ -10,6 +10,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import comm as OC
 from oracle import ring as OR
@@ -307,3 +308,47 @@ def test_host_ring_rejects_null_pointers_and_small_or_misaligned_workspace(cpa, 
     with pytest.raises(cpa.CpError) as e:  # workspace not 256-byte aligned
         cpa.cp_ring_attn_host(desc, *([FAKE] * 6), 4096 + 16, need, stream=0)
     assert e.value.status == 1
+
+
+def _ring_tensors(b=1, S=1024, hq=4, hkv=2, d=64):
+    q = torch.zeros((b, S, hq, d), dtype=torch.bfloat16)
+    k = torch.zeros((b, S, hkv, d), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    o = torch.zeros((b, S, hq, d), dtype=torch.float32)
+    m = torch.zeros((b, hq, S), dtype=torch.float32)
+    return [q, k, v, o, m, torch.zeros_like(m)]
+
+
+@pytest.mark.parametrize("bad", ["dtype", "layout", "size", "device"])
+def test_binding_checks_tensor_arguments(cpa, bad):
+    """The binding rejects a tensor the kernels would read or write out of bounds, before any call."""
+    desc = _desc(cpa, h_q=4, h_kv=2)
+    args = _ring_tensors()
+    if bad == "dtype":
+        args[0] = args[0].float()
+    elif bad == "layout":
+        args[3] = torch.zeros((1, 1024, 4, 128), dtype=torch.float32)[..., ::2]
+    elif bad == "size":
+        args[4] = args[4][:, :, :512]
+    # "device": host tensors passed to a device entry point
+    with pytest.raises(ValueError):
+        cpa.cp_ring_step_partial_attn(desc, 0, 2, *args, 0, stream=0)
+
+
+def test_binding_checks_merge_decode_and_host_ring_arguments(cpa):
+    o = torch.zeros((2, 1, 8, 2, 8), dtype=torch.float32)
+    ml = torch.zeros((2, 1, 2, 8), dtype=torch.float32)
+    oo = torch.zeros((1, 8, 2, 8), dtype=torch.float32)
+    mo = torch.zeros((1, 2, 8), dtype=torch.float32)
+    with pytest.raises(ValueError):  # too few parts in o_parts
+        cpa.cp_merge_partials(1, 8, 2, 8, 3, o, ml, ml, oo, mo, mo, stream=0)
+    with pytest.raises(ValueError):  # workspace smaller than the bytes passed
+        cpa.cp_merge_partials_tree(1, 8, 2, 8, 2, o, ml, ml, torch.zeros(4), 64, oo, mo, mo, stream=0)
+    ddesc = cpa.make_desc(1, 256, 2, 2, 128, 2, 0.1, 0)
+    q = torch.zeros((1, 2, 128), dtype=torch.bfloat16)
+    kv = torch.zeros((1, 256, 2, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # out must be fp32
+        cpa.cp_passq_decode(ddesc, q, kv, kv, FAKE, 1 << 20, torch.zeros((1, 2, 128), dtype=torch.bfloat16), stream=0)
+    with pytest.raises(ValueError):  # the host-buffer ring wants host tensors and a device workspace
+        cpa.cp_ring_attn_host(_desc(cpa, h_q=4, h_kv=2), *_ring_tensors(), torch.zeros(1 << 10, dtype=torch.uint8),
+                              1 << 10, stream=0)

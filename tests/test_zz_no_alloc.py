@@ -89,8 +89,8 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
     desc = cpa.make_desc(64, 4096, 64, 64, 512, 8, 1.0 / math.sqrt(512), 0)
     q = torch.zeros(16, dtype=torch.bfloat16, device="cuda")  # never read: rejected before any launch
     out = torch.zeros(16, dtype=torch.float32, device="cuda")
-    with pytest.raises(cpa.CpError) as e:
-        cpa.cp_passq_decode_noalloc(desc, q, q, q, out)
+    with pytest.raises(cpa.CpError) as e:  # raw addresses: the C ABI's own check, not the binding's
+        cpa.cp_passq_decode_noalloc(desc, q.data_ptr(), q.data_ptr(), q.data_ptr(), out.data_ptr())
     assert e.value.status == 2 and "scratch" in str(e.value)
     assert cpa.CP_PASSQ_NOALLOC_SCRATCH_BYTES == 8 << 20
     assert np.all(out.cpu().numpy() == 0)
