@@ -408,6 +408,82 @@ def test_passq_reduce_is_the_size_of_the_triples():
         assert reduce_ == o.nbytes + m.nbytes + l.nbytes
 
 
+def _simulate_kv_footprint(b, S, cp, c_kv, layers_local, layout="balanced"):
+    """Allocate the KV cache every rank holds under the chunk plan and count its bytes.
+
+    Rank r keeps, for each of its L_local layers and each of the b sequences, c_kv
+    bytes (K and V together) for every token of its two chunks.  Returns the bytes
+    held by each rank, counted from real arrays."""
+    C = S // (2 * cp)
+    held = []
+    for r in range(cp):
+        tokens = sum(C for _ in OR.rank_chunks(cp, layout)[r])
+        caches = [np.zeros((b, tokens, c_kv), dtype=np.uint8) for _ in range(layers_local)]
+        held.append(sum(a.nbytes for a in caches))
+    return held
+
+
+FOOTPRINT_CASES = [(1, 64, 1, 8, 1), (2, 96, 4, 3, 5), (3, 128, 8, 20, 2), (1, 256, 16, 16, 3), (4, 48, 2, 7, 4)]
+
+
+def check_kv_footprint(fn):
+    for b, S, cp, c_kv, L in FOOTPRINT_CASES:
+        held = _simulate_kv_footprint(b, S, cp, c_kv, L)
+        assert len(set(held)) == 1  # the balanced split gives every rank the same KV
+        assert fn(b, S, c_kv, L, cp) == held[0], (b, S, cp, c_kv, L)
+        seq = _simulate_kv_footprint(b, S, cp, c_kv, L, layout="sequential")
+        assert seq == held  # the layout moves tokens between chunks, never the per-rank count
+
+
+def test_kv_footprint_equals_allocated_cache():
+    # memory paragraph of the Algorithm / formulas section: b * S * c_kv * L_local / cp per rank
+    check_kv_footprint(OC.kv_bytes_per_rank)
+
+
+@pytest.mark.parametrize("kind", ["drop_b", "drop_layers", "drop_cp", "c_kv_per_k_only"])
+def test_footprint_pin_catches_planted_mistakes(kind):
+    def mutant(b, S, c_kv, L, cp):
+        if kind == "drop_b":
+            return S * c_kv * L // cp
+        if kind == "drop_layers":
+            return b * S * c_kv // cp
+        if kind == "drop_cp":
+            return b * S * c_kv * L
+        return b * S * (c_kv // 2) * L // cp
+    assert _fails(check_kv_footprint, mutant), f"planted footprint mistake {kind!r} slipped through"
+
+
+def _per_token_kv_bytes(h_kv, d_head, itemsize):
+    """c_kv counted from the K and V rows one token appends to the cache of one layer."""
+    dtype = {2: np.float16, 4: np.float32}[itemsize]
+    k_row = np.zeros((h_kv, d_head), dtype)
+    v_row = np.zeros((h_kv, d_head), dtype)
+    return k_row.nbytes + v_row.nbytes
+
+
+def test_c_kv_of_grouped_heads_equals_one_token_of_cache():
+    for h_kv, d_head, s in [(4, 64, 2), (8, 128, 2), (1, 512, 2), (8, 128, 4), (3, 5, 2)]:
+        assert OC.c_kv_gqa(h_kv, d_head, s) == _per_token_kv_bytes(h_kv, d_head, s)
+
+
+def test_workload_byte_counts_written_out():
+    # c_kv and eq. g5cp-passkv-bytes at the three prefill workloads, multiplied out by hand:
+    #   tiny  h_kv 4, d 64:   c_kv = 2*4*64*2  = 1024 B; M = 1 * 512 * 1024      = 524,288
+    #   gqa   h_kv 8, d 128:  c_kv = 2*8*128*2 = 4096 B; M = 7 * 4096 * 4096     = 117,440,512
+    #   long  h_kv 8, d 128:  c_kv = 4096 B;            M = 15 * 8192 * 4096     = 503,316,480
+    # and the 1M use case with the MLA c_kv of Appendix B: M = 7 * 131072 * 320 = 293,601,280.
+    assert OC.c_kv_gqa(4, 64, 2) == 1024
+    assert OC.c_kv_gqa(8, 128, 2) == 4096
+    assert OC.passkv_bytes(1024, 2, 1024) == (524_288, 524_288)
+    assert OC.passkv_bytes(32768, 8, 4096) == (117_440_512, 16_777_216)
+    assert OC.passkv_bytes(131072, 16, 4096) == (503_316_480, 33_554_432)
+    assert OC.passkv_bytes(1 << 20, 8, 320) == (293_601_280, 41_943_040)
+    # pass-Q at the decode workload (b 8, n_h 16, d = 16 * 512 = 8192):
+    #   dispatch 8*8192*2 = 131,072; reduce 8*(8192+32)*2 = 131,584 (s = 2), 263,168 (s = 4)
+    assert OC.passq_bytes(8, 8192, 16, 2) == (131_072, 131_584)
+    assert OC.passq_bytes(8, 8192, 16, 4) == (262_144, 263_168)
+
+
 def test_page_integers():
     g = json.load(open(GOLDEN))
     uc = g["use_case_prefill"]
