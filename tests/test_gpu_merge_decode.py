@@ -274,7 +274,7 @@ def test_shared_kv_decode_forced_rescales():
     out, mo, lo = _decode(q, k, v, cp)
     ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
     assert_out_close(out.cpu().numpy(), ref_out, "mqa rescale")
-    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS * 10
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
 
 
 def test_shared_kv_decode_workload_sampled():
@@ -347,9 +347,9 @@ def test_decode_scale_is_the_one_passed(case):
                                    (64, 3, 17, 2, 128), (13, 1, 16, 1, 128)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("finalize", [False, True])
-def test_tma_merge_gives_the_register_merges_bits(shape, finalize, monkeypatch):
+def test_tma_merge_gives_the_register_merges_bits(shape, finalize):
     """d = 128 and up to 64 parts take the TMA-fed merge; it folds the same parts in the same
-    order with the same arithmetic as the register-pipelined merge (CPATTN_MERGE_TMA=0)."""
+    order with the same arithmetic as the register-pipelined merge (merge-kernel knob 0)."""
     n, b, rows, heads, d = shape
     gen = torch.Generator(device="cpu").manual_seed(1000 + n + rows)
     o = torch.randn((n, b, rows, heads, d), generator=gen).cuda()
@@ -359,9 +359,12 @@ def test_tma_merge_gives_the_register_merges_bits(shape, finalize, monkeypatch):
     l[0, 0, 0, :3] = 0.0
     order = list(np.random.default_rng(n).permutation(n))
     got = {}
-    for tma in ("1", "0"):
-        monkeypatch.setenv("CPATTN_MERGE_TMA", tma)
-        got[tma] = _merge(o, m, l, order=order, finalize=finalize)
-        assert cpa.cp_take_device_status() == 0
+    try:
+        for tma in ("1", "0"):
+            cpa.cp_set_kernel_choice(cpa.CP_KNOB_MERGE_KERNEL, int(tma))
+            got[tma] = _merge(o, m, l, order=order, finalize=finalize)
+            assert cpa.cp_take_device_status() == 0
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_MERGE_KERNEL, -1)
     for x, y in zip(got["1"], got["0"]):
         assert torch.equal(x, y)
