@@ -26,6 +26,7 @@ __all__ = [
     "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
     "cp_merge_tree_workspace_bytes", "cp_merge_partials_tree", "cp_selftest_wait_timeout",
+    "cp_set_kernel_choice", "CP_KNOB_RING_PAIRING", "CP_KNOB_MERGE_KERNEL",
 ]
 
 CP_OK = 0
@@ -41,6 +42,8 @@ CP_LAYOUT_BALANCED = 0
 CP_LAYOUT_SEQUENTIAL = 1
 CP_MAX_MERGE_PARTS = 256
 CP_PASSQ_NOALLOC_SCRATCH_BYTES = 8 << 20
+CP_KNOB_RING_PAIRING = 0
+CP_KNOB_MERGE_KERNEL = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -105,6 +108,7 @@ def load_library():
                                           _I32, _P]),
         "cp_passq_decode_noalloc": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P]),
         "cp_selftest_wait_timeout": (_I32, [_P]),
+        "cp_set_kernel_choice": (_I32, [_I32, _I32]),
         "cp_ring_attn_host_workspace_bytes": (_I32, [ctypes.POINTER(AttnDesc), ctypes.POINTER(ctypes.c_size_t)]),
         "cp_ring_attn_host": (_I32, [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     }
@@ -125,11 +129,17 @@ def _ptr(x) -> Optional[int]:
     return x.data_ptr()
 
 
+def _current_device() -> int:
+    import torch
+    return torch.cuda.current_device()
+
+
 def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, cuda: bool = True) -> Optional[int]:
     """Address of a tensor argument, after the checks the C ABI cannot make through a plain
-    pointer: dtype, contiguity, size against the descriptor, and device.  A wrong buffer
-    would otherwise be read or written out of bounds by the kernels.  None and raw int
-    addresses pass through unchecked."""
+    pointer: dtype, contiguity, size against the descriptor, and device (CUDA tensors must
+    be on the current device, where the kernels run).  A wrong buffer would otherwise be
+    read or written out of bounds by the kernels.  None and raw int addresses pass
+    through unchecked."""
     if x is None or isinstance(x, int):
         return x
     if dtype is not None and x.dtype != dtype:
@@ -142,6 +152,9 @@ def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, 
         raise ValueError(f"{where}: {name} holds {x.numel() * x.element_size()} bytes, {nbytes} were passed")
     if bool(x.is_cuda) != cuda:
         raise ValueError(f"{where}: {name} must be a {'CUDA' if cuda else 'host (CPU)'} tensor")
+    if cuda and x.device.index != _current_device():
+        raise ValueError(f"{where}: {name} is on cuda:{x.device.index}, but the current device "
+                         f"(where the kernels run) is cuda:{_current_device()}")
     return x.data_ptr()
 
 
@@ -353,6 +366,12 @@ def cp_passq_decode_noalloc(desc: AttnDesc, q, k, v, out, m_out=None, l_out=None
         raise CpError(st, "cp_passq_decode_noalloc (unsupported shape, or partials larger than the "
                           f"{CP_PASSQ_NOALLOC_SCRATCH_BYTES >> 20} MiB fixed scratch)")
     _check(st, "cp_passq_decode_noalloc")
+
+
+def cp_set_kernel_choice(knob: int, value: int) -> None:
+    """Process-wide kernel choice for tests and diagnostics (-1 = automatic); every choice
+    computes the same bits."""
+    _check(load_library().cp_set_kernel_choice(int(knob), int(value)), "cp_set_kernel_choice")
 
 
 def cp_selftest_wait_timeout(stream=None) -> None:

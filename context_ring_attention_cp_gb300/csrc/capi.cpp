@@ -11,6 +11,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -22,6 +23,15 @@ cudaError_t cpattn::current_sm_count(int* sms) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+namespace {
+constexpr int kKnobs = 2;
+std::atomic<int32_t> g_kernel_choice[kKnobs] = {{-1}, {-1}};
+}  // namespace
+
+int32_t cpattn::kernel_choice(int32_t knob) {
+  return (knob >= 0 && knob < kKnobs) ? g_kernel_choice[knob].load(std::memory_order_relaxed) : -1;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 cpattn::tensor_map_encoder() {
@@ -550,6 +560,12 @@ cp_status cp_passq_decode_noalloc(const cp_attn_desc* desc, const void* q, const
   float* scratch = nullptr;
   if (decode_noalloc_scratch(&scratch) != cudaSuccess) return CP_ERR_CUDA;
   return run_passq_decode(*desc, splits, q, k, v, scratch, out, m_out, l_out, static_cast<cudaStream_t>(cuda_stream));
+}
+
+cp_status cp_set_kernel_choice(int32_t knob, int32_t value) {
+  if (knob < 0 || knob >= kKnobs || value < -1 || value > 1) return CP_ERR_INVALID_ARGUMENT;
+  g_kernel_choice[knob].store(value, std::memory_order_relaxed);
+  return CP_OK;
 }
 
 cp_status cp_selftest_wait_timeout(void* cuda_stream) {

@@ -16,6 +16,8 @@ namespace cpattn {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // SM count of the calling thread's current device.
 cudaError_t current_sm_count(int* sms);
+// Current value of a cp_set_kernel_choice knob (-1 = automatic).
+int32_t kernel_choice(int32_t knob);
 
 // ---- LSE merge (merge.cu) --------------------------------------------------
 struct MergeParams {
@@ -50,7 +52,7 @@ cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const 
                                    float* m_parts, float* l_parts, cudaStream_t stream);
 
 // Fixed 8 MiB device scratch used by cp_passq_decode_noalloc (decode.cu): its size,
-// and its device address on the current device (looked up once per device).
+// and its device address on the current device (looked up once per device and context).
 size_t decode_noalloc_scratch_bytes();
 cudaError_t decode_noalloc_scratch(float** ptr);
 

@@ -774,15 +774,6 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_
   return r == CUDA_SUCCESS;
 }
 
-// CPATTN_RING_PAIRING: "single" -> 0, "pair" -> 1, unset or anything else -> -1 (automatic).
-int32_t ring_pairing_override() {
-  const char* e = getenv("CPATTN_RING_PAIRING");
-  if (e == nullptr) return -1;
-  if (strcmp(e, "single") == 0) return 0;
-  if (strcmp(e, "pair") == 0) return 1;
-  return -1;
-}
-
 template <int D, int LAYOUT>
 cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
   using K = Cfg<D>;
@@ -825,11 +816,11 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   // With one query head per kv head, a launch whose single tiles fit in one wave runs one
   // tile per CTA (the head-pair form, which finds no second head): pairing would halve its
   // CTAs and lengthen each CTA's chain (a tiny prefill: 15.5 against 19.4 us).
-  // CPATTN_RING_PAIRING=single|pair overrides the choice; the results are the same bits.
+  // The CP_KNOB_RING_PAIRING setting overrides the choice; the results are the same bits.
   if (p.group == 1) {
     const int64_t n_single =
         int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.tpc * d.b * d.h_q;
-    const int32_t forced = ring_pairing_override();
+    const int32_t forced = kernel_choice(CP_KNOB_RING_PAIRING);
     int sms = 0;
     if (forced < 0 && current_sm_count(&sms) != cudaSuccess) return CP_ERR_CUDA;
     if (forced == 0 || (forced < 0 && n_single <= int64_t(sms))) row_pairs = false;

@@ -12,7 +12,8 @@
  * - Ownership: the caller allocates and owns every buffer and the CUDA stream.
  *   The library never allocates device memory, never frees, keeps no state
  *   between calls except the device status word read by
- *   cp_take_device_status(), and never synchronises a stream (except in
+ *   cp_take_device_status() and the kernel-choice settings of
+ *   cp_set_kernel_choice(), and never synchronises a stream (except in
  *   cp_take_device_status()).  Device calls are asynchronous on `cuda_stream`
  *   (a cudaStream_t; NULL = the legacy default stream).
  * - Errors are returned BEFORE any launch and nothing is launched on error;
@@ -127,8 +128,8 @@ CPATTN_API cp_status cp_plan_chunks(int64_t S, int32_t cp, int32_t layout, int64
  * Tiling: each CTA computes two 128-row query tiles that share every K/V tile: two
  * heads of one kv group (even h_q / h_kv) or two consecutive row tiles of one head
  * (odd).  With h_q == h_kv, a launch with at most one wave (SM count) of single tiles
- * keeps one tile per CTA; the environment variable CPATTN_RING_PAIRING=single|pair
- * overrides that choice at each call, and every choice gives the same bits.
+ * keeps one tile per CTA; cp_set_kernel_choice(CP_KNOB_RING_PAIRING, ...) overrides
+ * that choice, and every choice gives the same bits.
  * Supported: d in {64, 128}; causal = 1; every pointer 16-byte aligned.
  * Errors: cp < 1, S % (2cp) != 0, h_q % h_kv != 0, any size < 1, scale <= 0 or
  * not finite, 0 <= step_begin < step_end <= cp violated, unknown mode bits, NULL or
@@ -199,8 +200,9 @@ CPATTN_API cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_h
  * 0..n_parts-1; NULL = index order).  Parts with m_p = -inf weigh 0; a row whose
  * parts are all the identity stays the identity.  finalize != 0 writes O / l
  * (0 where l = 0) into o_out instead of O.  Outputs must not alias inputs.
- * With d = 128 and at most 64 parts the O rows are streamed by TMA; the environment
- * variable CPATTN_MERGE_TMA=0 selects the plain-load kernel, which gives the same bits.
+ * With d = 128 and at most 64 parts the O rows are streamed by TMA;
+ * cp_set_kernel_choice(CP_KNOB_MERGE_KERNEL, 0) selects the plain-load kernel, which
+ * gives the same bits.
  * A device-side wait that gives up records CP_ERR_TIMEOUT for cp_take_device_status.
  * Errors: any size < 1, n_parts > CP_MAX_MERGE_PARTS, d % 4 != 0, `order` not a
  * permutation, NULL or misaligned device pointer -> CP_ERR_INVALID_ARGUMENT;
@@ -283,7 +285,10 @@ CPATTN_API cp_status cp_passq_decode(const cp_attn_desc* desc, const void* q, co
  * - It calls no cudaMalloc, cudaFree or other allocating routine.
  * - The first call on a device looks up the scratch's device address (once per
  *   device, with that device current); make that first call before any stream
- *   capture.
+ *   capture.  Each call checks that the device's context is still the one the
+ *   address was looked up in; after a device reset (cudaDeviceReset) the next
+ *   call looks it up again in the new context, so that call too should come
+ *   before any capture.
  * - All calls share the scratch, which keeps the last call's contents (nothing in
  *   it needs to start at zero).  Calls that overlap on the GPU (other streams,
  *   or other host threads) race on it and must be serialised by the caller.
@@ -328,6 +333,21 @@ typedef struct {
  * result struct is then left untouched).
  */
 CPATTN_API cp_status cp_comm_bytes(const cp_comm_query* query, cp_comm_result* result);
+
+/*
+ * Kernel-choice settings, for tests and diagnostics (the pages have no counterpart:
+ * each knob picks between kernels of this library that compute the same bits).
+ *   CP_KNOB_RING_PAIRING  -1 automatic (default); 0 one query tile per CTA for
+ *                         launches with h_q == h_kv; 1 two tiles per CTA always.
+ *   CP_KNOB_MERGE_KERNEL  -1 automatic (default: TMA-fed where supported);
+ *                         0 the plain-load kernel; 1 the same as -1.
+ * The setting is process-wide, applies to every device and to launches made after
+ * the call returns, and is read once per launch (no environment variable is read
+ * anywhere in the library).
+ * Errors: an unknown knob or a value outside {-1, 0, 1} -> CP_ERR_INVALID_ARGUMENT.
+ */
+enum { CP_KNOB_RING_PAIRING = 0, CP_KNOB_MERGE_KERNEL = 1 };
+CPATTN_API cp_status cp_set_kernel_choice(int32_t knob, int32_t value);
 
 /*
  * Synchronise `cuda_stream`, then read and clear the library's device status

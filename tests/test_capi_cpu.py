@@ -139,11 +139,19 @@ def test_kv_per_rank_halves_from_cp8_to_cp16(cpa):
 
 
 def test_comm_bytes_at_the_workloads(cpa):
-    # c_kv for grouped-query attention: K and V, h_kv heads of d_head bf16 values
-    for S, cp, hkv, dh in [(1024, 2, 4, 64), (32768, 8, 8, 128), (131072, 16, 8, 128)]:
-        c_kv = OC.c_kv_gqa(hkv, dh, 2)
+    # c_kv = K and V, h_kv heads of d_head bf16 values: 2*4*64*2 = 1024 B (tiny) and
+    # 2*8*128*2 = 4096 B (gqa, long); eq. g5cp-passkv-bytes multiplied out by hand
+    for S, cp, c_kv, total, per_step in [(1024, 2, 1024, 524_288, 524_288),
+                                         (32768, 8, 4096, 117_440_512, 16_777_216),
+                                         (131072, 16, 4096, 503_316_480, 33_554_432)]:
         got = cpa.cp_comm_bytes(S, cp, c_kv)
-        assert got["passkv_total"] == OC.passkv_bytes(S, cp, c_kv)[0]
+        assert (got["passkv_total"], got["passkv_per_step"]) == (total, per_step)
+    # pass-Q at the decode workload: b 8, n_h 16, d = 16 * 512
+    got = cpa.cp_comm_bytes(131072, 8, 0, b=8, d=8192, n_h=16, s_dtype=2)
+    assert (got["passq_dispatch"], got["passq_reduce"]) == (131_072, 131_584)
+    # per-rank KV of the gqa workload over 36 layers: 1 * 32768 * 4096 * 36 / 8
+    got = cpa.cp_comm_bytes(32768, 8, 4096, b=1, layers_local=36)
+    assert got["kv_bytes_per_rank"] == 603_979_776
 
 
 def test_comm_bytes_overflow_and_errors(cpa):
@@ -352,3 +360,56 @@ def test_binding_checks_merge_decode_and_host_ring_arguments(cpa):
     with pytest.raises(ValueError):  # the host-buffer ring wants host tensors and a device workspace
         cpa.cp_ring_attn_host(_desc(cpa, h_q=4, h_kv=2), *_ring_tensors(), torch.zeros(1 << 10, dtype=torch.uint8),
                               1 << 10, stream=0)
+
+
+class _FakeCudaTensor:
+    """Stands in for a CUDA tensor on a chosen device (no GPU is needed to test the check)."""
+
+    def __init__(self, index, dtype=torch.float32, numel=64):
+        self.dtype, self.is_cuda, self._n = dtype, True, numel
+        self.device = torch.device("cuda", index)
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        return self._n
+
+    def element_size(self):
+        return 4
+
+    def data_ptr(self):
+        return 4096
+
+
+def test_binding_rejects_a_tensor_on_another_device(cpa, monkeypatch):
+    # kernels run on the current device: a tensor of another GPU must never reach them
+    monkeypatch.setattr(cpa, "_current_device", lambda: 0)
+    assert cpa._arg(_FakeCudaTensor(0), "o", "test", torch.float32, 64) == 4096
+    with pytest.raises(ValueError, match="cuda:1"):
+        cpa._arg(_FakeCudaTensor(1), "o", "test", torch.float32, 64)
+    desc = _desc(cpa, S=8, h_q=1, h_kv=1, d=8)
+    args = [_FakeCudaTensor(0, torch.bfloat16)] * 3 + [_FakeCudaTensor(0)] * 3
+    args[4] = _FakeCudaTensor(1)
+    with pytest.raises(ValueError, match="m is on cuda:1"):
+        cpa.cp_ring_step_partial_attn(desc, 0, 2, *args, 0, stream=0)
+
+
+def test_kernel_choice_settings(cpa):
+    lib = cpa.load_library()
+    for knob in (cpa.CP_KNOB_RING_PAIRING, cpa.CP_KNOB_MERGE_KERNEL):
+        for value in (-1, 0, 1, -1):
+            cpa.cp_set_kernel_choice(knob, value)
+        for bad in (-2, 2):
+            assert lib.cp_set_kernel_choice(knob, bad) == 1
+    for bad_knob in (-1, 2, 99):
+        with pytest.raises(cpa.CpError) as e:
+            cpa.cp_set_kernel_choice(bad_knob, 0)
+        assert e.value.status == 1
+
+
+def test_library_reads_no_environment_variable():
+    # kernel choices are explicit settings, never read from the caller's environment
+    import glob
+    for path in glob.glob(os.path.join(os.path.dirname(__file__), "..", "context_ring_attention_cp_gb300", "csrc", "*")):
+        assert "getenv" not in open(path).read(), path
