@@ -327,7 +327,7 @@ cudaError_t launch_decode_partials(const cp_attn_desc& d, int32_t splits, const 
 // output buffers, or a latency-bound token loop that must not call cudaMalloc
 // (which may synchronise the device).  For them the decode partials live in this
 // array instead of a caller workspace.  It is part of the module image, so every
-// GPU that loads the library holds kNoAllocScratchBytes until the process exits.
+// GPU that loads the library holds its 8 MiB until the process exits.
 // All calls share it and it keeps the last call's contents; nothing in it needs
 // to start at zero (every partial is written before the reduce reads it), and
 // calls that overlap on the GPU race on it.
@@ -339,27 +339,66 @@ static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+struct ScratchAddr {
+  unsigned long long ctx_id;  // the context the address belongs to
+  float* ptr;
+};
+ScratchAddr g_noalloc_addr[kMaxDevices] = {};
+
+// Id of the calling thread's current context, 0 when it cannot be read.  A device
+// reset destroys the context that holds the array; the next context has a new id.
+unsigned long long current_context_id() {
+  struct Fns {
+    PFN_cuCtxGetCurrent_v4000 get_current;
+    PFN_cuCtxGetId_v12000 get_id;
+  };
+  static const Fns fns = []() {
+    Fns f{nullptr, nullptr};
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.get_current == nullptr || fns.get_id == nullptr || fns.get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || fns.get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 }  // namespace
 
 size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchFloats * sizeof(float); }
 
-// The array's name in host code is only a host-side stand-in; the device
-// address is looked up once per device, with that device current.
+// The array's name in host code is only a host-side stand-in; its device address is
+// looked up with the device current, once per device and context: the first call on
+// a device does it, and so does the first call after a device reset.
 cudaError_t decode_noalloc_scratch(float** ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // Makes the device's primary context current (and creates it if a reset destroyed
+  // it), so that the id read below is the context the kernels will run in.
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  ScratchAddr& a = g_noalloc_addr[dev];
+  if (a.ptr == nullptr || ctx == 0 || ctx != a.ctx_id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    a.ptr = static_cast<float*>(p);
+    a.ctx_id = ctx;
   }
-  *ptr = g_noalloc_ptr[dev];
+  *ptr = a.ptr;
   return cudaSuccess;
 }
 
