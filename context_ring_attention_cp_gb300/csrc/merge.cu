@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 4) lse_merge_tma_kernel(const __grid
                 int32_t(int64_t(p.order[kpos]) * p.batch + bi));
   };
   // The first parts stream in while the m and l scalars are staged.
+  int issued = 0;  // copies issued (thread 0 only)
   if (threadIdx.x == 0) {
     for (int sl = 0; sl < kTmaSlots; ++sl) {
       mbar_init(full(sl), 1);
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 4) lse_merge_tma_kernel(const __grid
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int kpos = 0; kpos < n_parts && kpos < kTmaSlots; ++kpos) issue(kpos);
+    issued = n_parts < kTmaSlots ? n_parts : kTmaSlots;
   }
   for (int idx = threadIdx.x; idx < n_parts * kRowsPerCta; idx += kThreads) {
     const int kpos = idx / kRowsPerCta;
@@ -270,16 +272,23 @@ __global__ void __launch_bounds__(kThreads, 4) lse_merge_tma_kernel(const __grid
         ok = false;
       } else {
         issue(kpos + kTmaSlots);
+        ++issued;
       }
     }
     if (!__all_sync(0xffffffffu, ok)) break;
   }
   if (!ok || *abort_flag) {
-    // Thread 0 issued every copy: it stays until those in flight have landed, which
-    // keeps the CTA's shared memory allocated; the other threads leave at once.
+    // Thread 0 issued every copy: before it leaves, it waits for the last copy issued
+    // into each slot to land (its full barrier's phase to complete), which keeps the
+    // CTA's shared memory allocated meanwhile; the other threads leave at once.  The
+    // wait is bounded (10 ms for all slots): a copy later than that is not waited for.
     if (threadIdx.x == 0) {
       const uint64_t t0 = globaltimer();
-      while (globaltimer() - t0 < 50000ull) {
+      for (int kpos = issued > kTmaSlots ? issued - kTmaSlots : 0; kpos < issued; ++kpos) {
+        const uint32_t bar = full(kpos % kTmaSlots);
+        const uint32_t ph = uint32_t((kpos / kTmaSlots) & 1);
+        while (!mbar_try_wait(bar, ph) && globaltimer() - t0 < 10000000ull) {
+        }
       }
     }
     return;
@@ -307,10 +316,7 @@ __global__ void __launch_bounds__(kThreads, 4) lse_merge_tma_kernel(const __grid
   }
 }
 
-bool merge_tma_enabled() {
-  const char* e = getenv("CPATTN_MERGE_TMA");
-  return e == nullptr || strcmp(e, "0") != 0;
-}
+bool merge_tma_enabled() { return kernel_choice(CP_KNOB_MERGE_KERNEL) != 0; }
 
 // rows == 1 (the decode reduce: one triple per sequence and head).  One CTA per
 // (batch, head, slice of 128 columns), so the grid has batch * heads * ceil(d/128)
