@@ -17,9 +17,11 @@ during the timed region, and secondary lines for pass-Q decode (GB/s) and the
 LSE merge (GB/s).
 
 ``--impl reference`` times the CPU oracle (fp64, test infrastructure) on a
-bounded row sample of the same workload on the host cores.  The decode and merge
-secondary lines carry the oracle timed the same way on a bounded sample of their
-own inputs (unless --skip-cpu).
+bounded row sample of the same workload on the host cores.  The headline line and
+the tiny, long, decode and merge secondary lines each carry the oracle timed on the
+same inputs (the whole tiny workload; bounded samples of the others, with the
+full-workload time extrapolated from them) on a spawn pool of one single-threaded
+worker per host core (unless --skip-cpu).
 """
 
 from __future__ import annotations
@@ -71,9 +73,9 @@ def merge_bytes(w):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# ring kernel on this workload, from the ncu capture summarised in
-# profiles/ring_attn_gqa_ncu_full.md.  It is reported only while ring_attn.cu is
-# the source that was captured (sha256 prefix below); otherwise traffic is null.
+# ring kernel on this workload, from the ncu capture of that kernel.  It is reported
+# only while ring_attn.cu is the source that was captured (sha256 prefix below);
+# otherwise traffic is null.
 RING_TRAFFIC = {"sha256_prefix": "c9d394c7b0694ff1", "bytes": 893814272}
 
 
@@ -154,86 +156,8 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle (test infrastructure) on a bounded row sample
+# CPU oracle (test infrastructure) on bounded samples, on all of the host's cores
 # ---------------------------------------------------------------------------
-
-def _oracle_rows_task(args):
-    """One worker: causal attention for sampled rows of one head (fp64 oracle)."""
-    qbits, kbits, vbits, rows, scale = args
-    sys.path.insert(0, ROOT)
-    import oracle
-    from oracle import attention as OA
-    q = oracle.bf16_bits_to_f64(qbits)   # [R, d] rows of this head
-    k = oracle.bf16_bits_to_f64(kbits)   # [S, d] of its kv head
-    v = oracle.bf16_bits_to_f64(vbits)
-    S, d = k.shape
-    t0 = time.perf_counter()
-    qfull = np.zeros((1, S, 1, d))
-    qfull[0, rows, 0] = q
-    OA.causal_attention_rows(qfull, k[None, :, None], v[None, :, None], scale, 0, [0], rows)
-    dt = time.perf_counter() - t0
-    flops = sum(4 * d * (i + 1) for i in rows)
-    return flops, dt
-
-
-def oracle_sample_tasks(w, q, k, v, rows_per_head, heads, seed):
-    from context_ring_attention_cp_gb300 import synth
-    rng = np.random.default_rng(seed)
-    g = w["h_q"] // w["h_kv"]
-    tasks = []
-    for h in heads:
-        rows = sorted(int(x) for x in rng.integers(0, w["S"], size=rows_per_head))
-        kh = h // g
-        tasks.append((synth.bf16_bits(q[0, rows, h]), synth.bf16_bits(k[0, :, kh]), synth.bf16_bits(v[0, :, kh]),
-                      rows, 1.0 / math.sqrt(w["d"])))
-    return tasks
-
-
-def _oracle_decode_task(args):
-    """One worker: pass-Q decode of one (sequence, head) over all its keys (fp64 oracle)."""
-    qbits, kbits, vbits, scale = args
-    sys.path.insert(0, ROOT)
-    import oracle
-    from oracle import attention as OA
-    q = oracle.bf16_bits_to_f64(qbits)   # [d]
-    k = oracle.bf16_bits_to_f64(kbits)   # [L, d]
-    v = oracle.bf16_bits_to_f64(vbits)
-    t0 = time.perf_counter()
-    OA.decode_attention(q[None, None], k[None, :, None], v[None, :, None], scale)
-    dt = time.perf_counter() - t0
-    return 2 * k.size * 2, dt  # the bf16 K and V bytes this decode reads
-
-
-def _oracle_merge_task(args):
-    """One worker: the fold of n parts over some rows of one head (fp64 oracle)."""
-    m_parts, l_parts, o_parts = args     # [n, R], [n, R], [n, R, d] fp32
-    sys.path.insert(0, ROOT)
-    from oracle import ring as OR
-    n, R, d = o_parts.shape
-    parts = [(m_parts[p].astype(np.float64), l_parts[p].astype(np.float64), o_parts[p].astype(np.float64))
-             for p in range(n)]
-    t0 = time.perf_counter()
-    OR.merge_in_order(parts)
-    dt = time.perf_counter() - t0
-    return (n + 1) * R * (d + 2) * 4, dt  # the parts read and the triple written, in fp32 bytes
-
-
-def run_oracle_each(fn, tasks):
-    """Runs one task per single-threaded spawn worker, all at once; each worker times
-    its own task, so moving the inputs to the workers is not counted.  Returns the
-    tasks' bytes over the slowest worker's time (bytes/s) and that time."""
-    import multiprocessing as mp
-    os.environ["CPATTN_ORACLE_WORKER"] = "1"
-    try:
-        ctx = mp.get_context("spawn")
-        with ctx.Pool(len(tasks)) as pool:
-            pool.map(_oracle_warm, range(len(tasks)))
-            res = pool.map(fn, tasks)
-    finally:
-        os.environ.pop("CPATTN_ORACLE_WORKER", None)
-    slowest = max(r[1] for r in res)
-    return sum(r[0] for r in res) / slowest, slowest
-
 
 def _oracle_warm(_):
     sys.path.insert(0, ROOT)
@@ -241,21 +165,178 @@ def _oracle_warm(_):
     return 0
 
 
-def run_oracle_pool(tasks, workers):
-    """Times the oracle over ``tasks`` on a spawn pool of single-threaded workers."""
-    import multiprocessing as mp
-    os.environ["CPATTN_ORACLE_WORKER"] = "1"
-    try:
-        ctx = mp.get_context("spawn")
-        with ctx.Pool(workers) as pool:
-            pool.map(_oracle_warm, range(workers))  # imports happen outside the timed map
-            t0 = time.perf_counter()
-            res = pool.map(_oracle_rows_task, tasks)
-            wall = time.perf_counter() - t0
-    finally:
-        os.environ.pop("CPATTN_ORACLE_WORKER", None)
-    flops = sum(r[0] for r in res)
-    return flops, wall
+def _load(path):
+    return np.load(path, mmap_mode="r")
+
+
+def _oracle_prefill_rows_task(args):
+    """One task: causal attention of some sampled rows of one query head (fp64 oracle).
+    The inputs are bf16 bit files: the sampled Q rows [R, h_q, d] and K, V [S, h_kv, d]."""
+    qpath, kpath, vpath, h, kh, rows, sel, scale = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from oracle import attention as OA
+    t0 = time.perf_counter()
+    k = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(kpath)[:, kh, :]))
+    v = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(vpath)[:, kh, :]))
+    S, d = k.shape
+    qfull = np.zeros((1, S, 1, d))
+    qfull[0, rows, 0] = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(qpath)[sel, h, :]))
+    OA.causal_attention_rows(qfull, k[None, :, None], v[None, :, None], scale, 0, [0], rows)
+    return sum(4 * d * (i + 1) for i in rows), len(rows), time.perf_counter() - t0
+
+
+def _oracle_decode_shard_task(args):
+    """One task: the pass-Q partial triple of one (sequence, head) over one KV shard (fp64
+    oracle).  The inputs are bf16 bit files: q [d], and the shard's K, V rows [n, d]."""
+    qpath, kpath, vpath, scale = args
+    sys.path.insert(0, ROOT)
+    import oracle
+    from oracle import attention as OA
+    t0 = time.perf_counter()
+    q = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(qpath)))
+    k = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(kpath)))
+    v = oracle.bf16_bits_to_f64(np.ascontiguousarray(_load(vpath)))
+    OA.decode_shard_triples(q[None, None], k[None, :, None], v[None, :, None], scale, 1)
+    return 2 * k.size * 2, 1, time.perf_counter() - t0  # the bf16 K and V bytes this shard reads
+
+
+def _oracle_merge_task(args):
+    """One task: the fold of n parts over a block of rows of one head (fp64 oracle).
+    The inputs are fp32 files: m, l [n, R] and O [n, R, d] of that head."""
+    mpath, lpath, opath, r0, r1 = args
+    sys.path.insert(0, ROOT)
+    from oracle import ring as OR
+    t0 = time.perf_counter()
+    m, l, o = _load(mpath), _load(lpath), _load(opath)
+    n, _, d = o.shape
+    parts = [(np.asarray(m[p, r0:r1], np.float64), np.asarray(l[p, r0:r1], np.float64),
+              np.asarray(o[p, r0:r1], np.float64)) for p in range(n)]
+    OR.merge_in_order(parts)
+    return (n + 1) * (r1 - r0) * (d + 2) * 4, r1 - r0, time.perf_counter() - t0  # fp32 parts read + triple written
+
+
+class OraclePool:
+    """A spawn pool of single-threaded oracle workers, one per host core, created once and
+    shared by every CPU leg.  Inputs reach the workers as memory-mapped .npy files in a
+    temporary directory (removed on close), so nothing large is pickled."""
+
+    def __init__(self, workers):
+        import multiprocessing as mp
+        self.workers = int(workers)
+        self.dir = tempfile.TemporaryDirectory(prefix="cpattn_oracle_")
+        self._n = 0
+        os.environ["CPATTN_ORACLE_WORKER"] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.workers)
+        finally:
+            os.environ.pop("CPATTN_ORACLE_WORKER", None)
+        self.pool.map(_oracle_warm, range(self.workers))  # imports happen before any timing
+
+    def save(self, arr):
+        self._n += 1
+        path = os.path.join(self.dir.name, f"a{self._n}.npy")
+        np.save(path, np.ascontiguousarray(arr))
+        return path
+
+    def run(self, fn, tasks):
+        """All tasks at once over the pool: (total work, total rows or units, wall seconds)."""
+        t0 = time.perf_counter()
+        res = self.pool.map(fn, tasks, chunksize=1)
+        wall = time.perf_counter() - t0
+        return sum(r[0] for r in res), sum(r[1] for r in res), wall
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.dir.cleanup()
+
+    def describe(self):
+        return {"cores": self.workers, "host_cpus": os.cpu_count()}
+
+
+def oracle_prefill_leg(pool, w, q, k, v, heads, n_random, seed, full_rows=False):
+    """The oracle on sampled rows (or every row) of a prefill workload; b = 1.
+
+    Sample (per head in ``heads``): the first and last row of each of the 2cp chunks, rows 0
+    and S-1, and ``n_random`` seeded random rows; ``full_rows`` takes every row instead.
+    Returns the cpu_baseline object: fp64 TFLOP/s, rows/s and the full-config time."""
+    from context_ring_attention_cp_gb300 import synth
+    S, d, g = w["S"], w["d"], w["h_q"] // w["h_kv"]
+    rows = list(range(S)) if full_rows else synth.sample_rows(S, w["cp"], n_random, seed)
+    qpath = pool.save(synth.bf16_bits(q[0, rows]))
+    kpath = pool.save(synth.bf16_bits(k[0]))
+    vpath = pool.save(synth.bf16_bits(v[0]))
+    # split each head's rows so that every worker gets work of about the same size
+    per_head = max(1, (2 * pool.workers + len(heads) - 1) // len(heads))
+    tasks = []
+    for h in heads:
+        for part in range(per_head):
+            sel = list(range(part, len(rows), per_head))
+            if sel:
+                tasks.append((qpath, kpath, vpath, h, h // g, [rows[i] for i in sel], sel, 1.0 / math.sqrt(d)))
+    flops, nrows, wall = pool.run(_oracle_prefill_rows_task, tasks)
+    rate = flops / wall
+    full_flops = prefill_flops(w)
+    out = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "kind": "oracle", **pool.describe(),
+           "rows_per_s": round(nrows / wall, 1), "seconds": round(wall, 3)}
+    if full_rows and len(heads) == w["h_q"]:
+        out["full_config_s"] = {"value": round(wall, 3), "how": "measured (every row of every head)"}
+        out["sample"] = (f"the whole workload: {len(heads)} heads x {S} causal rows (fp64 numpy), "
+                         f"{len(tasks)} tasks on {pool.workers} single-threaded spawn workers")
+    else:
+        out["full_config_s"] = {"value": round(full_flops / rate, 1),
+                                "how": "extrapolated: the workload's FLOPs / the sample's fp64 FLOP rate"}
+        out["sample"] = (f"{len(heads)} heads x {len(rows)} rows (first and last row of each chunk, rows 0 and "
+                         f"S-1, {n_random} seeded random rows; causal, fp64 numpy), {len(tasks)} tasks on "
+                         f"{pool.workers} single-threaded spawn workers")
+    return out
+
+
+def oracle_decode_leg(pool, w, q, k, v, pairs):
+    """The oracle's pass-Q shard triples for the sampled (sequence, head) pairs, every shard
+    of each pair a task; GB/s of bf16 K/V read, and the full-config time extrapolated."""
+    from context_ring_attention_cp_gb300 import synth
+    L, cp, d, g = w["S"], w["cp"], w["d"], w["h_q"] // w["h_kv"]
+    n = L // cp
+    tasks = []
+    for bi, h in pairs:
+        qpath = pool.save(synth.bf16_bits(q[bi, h]))
+        for s in range(cp):
+            kpath = pool.save(synth.bf16_bits(k[bi, s * n:(s + 1) * n, h // g]))
+            vpath = pool.save(synth.bf16_bits(v[bi, s * n:(s + 1) * n, h // g]))
+            tasks.append((qpath, kpath, vpath, 1.0 / math.sqrt(d)))
+    nbytes, _, wall = pool.run(_oracle_decode_shard_task, tasks)
+    rate = nbytes / wall
+    full = 2 * w["b"] * L * w["h_q"] * d * 2
+    return {"value": round(rate / 1e9, 4), "unit": "GB/s", "kind": "oracle", **pool.describe(),
+            "seconds": round(wall, 3),
+            "full_config_s": {"value": round(full / rate, 2),
+                              "how": "extrapolated: all (sequence, head) pairs' K/V bytes / the sample's rate"},
+            "sample": f"{len(pairs)} (sequence, head) pairs x {cp} shards of {n} keys (fp64 numpy shard triples), "
+                      f"{len(tasks)} tasks on {pool.workers} single-threaded spawn workers"}
+
+
+def oracle_merge_leg(pool, w, po, pm, pl, heads):
+    """The oracle's left fold over all parts for every row of the sampled heads, in row
+    blocks; GB/s of fp32 triples read and written, and the full-config time extrapolated."""
+    R = w["rows"]
+    blocks = max(1, (2 * pool.workers + len(heads) - 1) // len(heads))
+    step = (R + blocks - 1) // blocks
+    tasks = []
+    for h in heads:
+        mpath = pool.save(pm[:, 0, h, :].cpu().numpy())
+        lpath = pool.save(pl[:, 0, h, :].cpu().numpy())
+        opath = pool.save(po[:, 0, :, h].cpu().numpy())
+        tasks += [(mpath, lpath, opath, r0, min(R, r0 + step)) for r0 in range(0, R, step)]
+    nbytes, _, wall = pool.run(_oracle_merge_task, tasks)
+    rate = nbytes / wall
+    return {"value": round(rate / 1e9, 4), "unit": "GB/s", "kind": "oracle", **pool.describe(),
+            "seconds": round(wall, 3),
+            "full_config_s": {"value": round(merge_bytes(w) / rate, 2),
+                              "how": "extrapolated: the workload's bytes / the sample's rate"},
+            "sample": f"{len(heads)} heads x {R} rows x {w['parts']} parts (fp64 numpy fold), {len(tasks)} tasks on "
+                      f"{pool.workers} single-threaded spawn workers"}
 
 
 # ---------------------------------------------------------------------------
@@ -296,6 +377,9 @@ def bench_ours(args, rank, world, dist):
     import context_ring_attention_cp_gb300 as cpa
     from context_ring_attention_cp_gb300 import _build, synth
 
+    # the oracle's worker pool (spawned, one single-threaded worker per host core) is made
+    # before the first GPU call and shared by every CPU leg
+    pool = OraclePool(args.cpu_workers) if (rank == 0 and not args.skip_cpu) else None
     if rank == 0 or world == 1:
         _build.build()
     if dist is not None:
@@ -401,18 +485,13 @@ def bench_ours(args, rank, world, dist):
 
     secondary = {}
     if not args.skip_secondary and rank == 0:
-        secondary = secondary_lines(cpa, synth, peaks, stream, cpu_legs=not args.skip_cpu)
+        secondary = secondary_lines(cpa, synth, peaks, stream, pool=pool)
 
     cpu = None
-    if rank == 0 and not args.skip_cpu:
-        tasks = oracle_sample_tasks(w, q, k, v, args.cpu_rows, list(range(0, hq, max(1, hq // args.cpu_workers)))[
-            :args.cpu_workers], seed=w["seed"])
-        cpu_flops, cpu_s = run_oracle_pool(tasks, args.cpu_workers)
-        cpu = {"value": round(cpu_flops / cpu_s / 1e12, 6), "unit": "TFLOP/s", "cores": args.cpu_workers,
-               "kind": "oracle",
-               "sample": f"{len(tasks)} heads x {args.cpu_rows} random rows of the {WORKLOAD} workload "
-                         f"(causal rows, fp64 numpy), {cpu_s:.1f} s on a spawn pool of {args.cpu_workers} "
-                         "single-threaded workers"}
+    if pool is not None:
+        # every head x the sampled rows of this workload (the inputs timed above)
+        cpu = oracle_prefill_leg(pool, w, q, k, v, list(range(hq)), args.cpu_random_rows, seed=w["seed"])
+        pool.close()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -428,7 +507,7 @@ def bench_ours(args, rank, world, dist):
     return line
 
 
-def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
+def secondary_lines(cpa, synth, peaks, stream, pool=None):
     import torch
     out = {}
     # one ring step (t = 1) of all cp virtual ranks on the GQA workload, EMIT: the spec's
@@ -521,6 +600,10 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
     out["prefill_long"] = {"workload": "prefill ring attention, long: b1, 32/8 heads, d128, S131072, cp16",
                            "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 3), "flops": prefill_flops(w),
                            "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+    if pool is not None:  # one query head per kv head x the sampled rows
+        g = w["h_q"] // w["h_kv"]
+        out["prefill_long"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(0, w["h_q"], g)), 64,
+                                                                 seed=w["seed"])
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # multi-head prefill: b1, 32/32 heads, d128, S32768, cp8 (the GQA workload's FLOPs with
@@ -570,6 +653,9 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
                            "us_in_cuda_graph": round(ms_graph * 1e3, 2),
                            "flops": prefill_flops(w), "peak": peaks["bf16_tflops"],
                            "frac": round(tf / peaks["bf16_tflops"], 4)}
+    if pool is not None:  # the whole workload: every row of every head
+        out["prefill_tiny"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(w["h_q"])), 0,
+                                                                 seed=w["seed"], full_rows=True)
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)
@@ -587,15 +673,9 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
     out["decode"] = {"workload": "pass-Q decode: b8, 16 heads, d512, L131072, cp8", "value": round(gbs, 1),
                      "unit": "GB/s", "ms": round(ms, 4), "bytes": decode_bytes(w), "peak": peaks["hbm_gbs"],
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": 2}
-    if cpu_legs:  # the oracle on 4 (sequence, head) pairs of the same inputs, one per worker
-        pairs = [(0, 0), (3, 5), (5, 10), (7, 15)]
-        tasks = [(synth.bf16_bits(q[bi, h]), synth.bf16_bits(k[bi, :, h]), synth.bf16_bits(v[bi, :, h]),
-                  1.0 / math.sqrt(w["d"])) for bi, h in pairs]
-        rate, slowest = run_oracle_each(_oracle_decode_task, tasks)
-        out["decode"]["cpu_baseline"] = {
-            "value": round(rate / 1e9, 4), "unit": "GB/s", "cores": len(tasks), "kind": "oracle",
-            "sample": f"{len(tasks)} (sequence, head) pairs, all 131072 keys each (fp64 numpy decode), one per "
-                      f"single-threaded spawn worker; slowest worker {slowest:.2f} s"}
+    if pool is not None:  # 16 (sequence, head) pairs, two per sequence, every shard of each
+        pairs = [(bi, h) for bi in range(w["b"]) for h in (bi % w["h_q"], (bi + 8) % w["h_q"])]
+        out["decode"]["cpu_baseline"] = oracle_decode_leg(pool, w, q, k, v, pairs)
     del q, k, v, ws
     torch.cuda.empty_cache()
     # pass-Q decode with 16 query heads sharing one 512-wide K/V head (MQA / MLA-style), tensor cores
@@ -634,15 +714,8 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
     out["merge"] = {"workload": "LSE merge: 32 parts x 64 heads x 4096 rows x 128", "value": round(gbs, 1),
                     "unit": "GB/s", "ms": round(ms, 4), "bytes": merge_bytes(w), "peak": peaks["hbm_gbs"],
                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    if cpu_legs:  # the oracle's fold over all rows of 4 heads of the same parts, one head per worker
-        R = w["rows"]
-        tasks = [(pm[:, 0, h, :R].cpu().numpy(), pl[:, 0, h, :R].cpu().numpy(), po[:, 0, :R, h].cpu().numpy())
-                 for h in (0, 21, 42, 63)]
-        rate, slowest = run_oracle_each(_oracle_merge_task, tasks)
-        out["merge"]["cpu_baseline"] = {
-            "value": round(rate / 1e9, 4), "unit": "GB/s", "cores": len(tasks), "kind": "oracle",
-            "sample": f"{len(tasks)} heads x {R} rows x {w['parts']} parts (fp64 numpy fold), one head per "
-                      f"single-threaded spawn worker; slowest worker {slowest:.3f} s"}
+    if pool is not None:  # every row of 16 of the 64 heads
+        out["merge"]["cpu_baseline"] = oracle_merge_leg(pool, w, po, pm, pl, list(range(0, w["heads"], 4)))
     # the same 32 parts reduced as the log-depth halving tree (5 levels of pairwise
     # merges), computed in one pass
     nbytes = cpa.cp_merge_tree_workspace_bytes(1, w["rows"], w["heads"], w["d"], w["parts"])
@@ -661,34 +734,41 @@ def secondary_lines(cpa, synth, peaks, stream, cpu_legs=False):
 
 
 def bench_reference(args, rank, world):
-    """The CPU oracle as the reference arm: bounded row samples of the same workload."""
+    """The CPU oracle as the reference arm: each step is the oracle over a bounded row sample
+    of the same workload (every head x the first and last row of each chunk, rows 0 and
+    S-1 and seeded random rows, a new draw each step) on a spawn pool of one
+    single-threaded worker per host core."""
     if rank != 0:
         return None
-    import torch
     from context_ring_attention_cp_gb300 import synth
     w = synth.WORKLOADS[WORKLOAD]
-    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"],
-                                   device="cpu")
-    heads = list(range(0, w["h_q"], max(1, w["h_q"] // args.cpu_workers)))[:args.cpu_workers]
-    rows = max(4, args.cpu_rows // 8)
-    for i in range(args.warmup):
-        run_oracle_pool(oracle_sample_tasks(w, q, k, v, rows, heads, seed=i), args.cpu_workers)
-    tot_flops, tot_s = 0, 0.0
-    for i in range(args.steps):
-        f, s = run_oracle_pool(oracle_sample_tasks(w, q, k, v, rows, heads, seed=1000 + i), args.cpu_workers)
-        tot_flops += f
-        tot_s += s
+    pool = OraclePool(args.cpu_workers)
+    try:
+        q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"],
+                                       device="cpu")
+        heads = list(range(w["h_q"]))
+        for i in range(args.warmup):
+            oracle_prefill_leg(pool, w, q, k, v, heads, args.cpu_random_rows, seed=i)
+        legs = [oracle_prefill_leg(pool, w, q, k, v, heads, args.cpu_random_rows, seed=1000 + i)
+                for i in range(args.steps)]
+    finally:
+        pool.close()
+    tot_s = sum(x["seconds"] for x in legs)
+    tot_flops = sum(x["value"] * 1e12 * x["seconds"] for x in legs)
     value = tot_flops / tot_s / 1e12
-    sample = (f"per step {len(heads)} heads x {rows} random rows (causal, fp64 numpy oracle) on a spawn pool of "
-              f"{args.cpu_workers} single-threaded workers")
+    cpu = dict(legs[-1])
+    cpu["value"] = round(value, 6)
+    cpu["seconds"] = round(tot_s, 3)
+    cpu["full_config_s"] = {"value": round(prefill_flops(w) / (value * 1e12), 1),
+                            "how": "extrapolated: the workload's FLOPs / the samples' fp64 FLOP rate"}
+    cpu["sample"] = f"per step: {legs[-1]['sample']}"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V)",
             "config": {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
                        "b": w["b"], "S": w["S"], "h_q": w["h_q"], "h_kv": w["h_kv"], "d": w["d"], "cp": w["cp"]},
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": args.cpu_workers,
-                             "kind": "oracle", "sample": sample},
+            "cpu_baseline": cpu,
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -777,8 +857,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-workers", type=int, default=min(16, os.cpu_count() or 1))
-    ap.add_argument("--cpu-rows", type=int, default=1536)
+    ap.add_argument("--cpu-workers", type=int, default=os.cpu_count() or 1,
+                    help="oracle worker processes (default: every host core)")
+    ap.add_argument("--cpu-random-rows", type=int, default=64,
+                    help="seeded random rows per head in the oracle's prefill sample")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
