@@ -26,7 +26,7 @@ __all__ = [
     "cp_ring_rank_partial_attn", "cp_merge_partials", "CP_LAYOUT_BALANCED", "CP_LAYOUT_SEQUENTIAL",
     "cp_passq_workspace_bytes", "cp_passq_decode", "cp_passq_decode_noalloc", "cp_take_device_status",
     "cp_merge_tree_workspace_bytes", "cp_merge_partials_tree", "cp_selftest_wait_timeout",
-    "cp_set_kernel_choice", "CP_KNOB_RING_PAIRING", "CP_KNOB_MERGE_KERNEL",
+    "cp_set_kernel_choice", "CP_KNOB_RING_PAIRING", "CP_KNOB_MERGE_KERNEL", "CP_KNOB_RING_KV_SPLIT",
 ]
 
 CP_OK = 0
@@ -44,6 +44,7 @@ CP_MAX_MERGE_PARTS = 256
 CP_PASSQ_NOALLOC_SCRATCH_BYTES = 8 << 20
 CP_KNOB_RING_PAIRING = 0
 CP_KNOB_MERGE_KERNEL = 1
+CP_KNOB_RING_KV_SPLIT = 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -134,61 +135,73 @@ def _current_device() -> int:
     return torch.cuda.current_device()
 
 
-def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, cuda: bool = True) -> Optional[int]:
+def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, cuda: bool = True,
+         dev: Optional[list] = None) -> Optional[int]:
     """Address of a tensor argument, after the checks the C ABI cannot make through a plain
     pointer: dtype, contiguity, size against the descriptor, and device (CUDA tensors must
     be on the current device, where the kernels run).  A wrong buffer would otherwise be
     read or written out of bounds by the kernels.  None and raw int addresses pass
-    through unchecked."""
+    through unchecked.  ``dev`` is a one-element list that caches the current device
+    across the arguments of one call."""
     if x is None or isinstance(x, int):
         return x
     if dtype is not None and x.dtype != dtype:
         raise ValueError(f"{where}: {name} must be {dtype}, got {x.dtype}")
     if not x.is_contiguous():
         raise ValueError(f"{where}: {name} must be contiguous")
-    if x.numel() < numel:
-        raise ValueError(f"{where}: {name} holds {x.numel()} elements, the descriptor needs {numel}")
-    if x.numel() * x.element_size() < nbytes:
-        raise ValueError(f"{where}: {name} holds {x.numel() * x.element_size()} bytes, {nbytes} were passed")
-    if bool(x.is_cuda) != cuda:
+    n = x.numel()
+    if n < numel:
+        raise ValueError(f"{where}: {name} holds {n} elements, the descriptor needs {numel}")
+    if nbytes and n * x.element_size() < nbytes:
+        raise ValueError(f"{where}: {name} holds {n * x.element_size()} bytes, {nbytes} were passed")
+    if x.is_cuda != cuda:
         raise ValueError(f"{where}: {name} must be a {'CUDA' if cuda else 'host (CPU)'} tensor")
-    if cuda and x.device.index != _current_device():
-        raise ValueError(f"{where}: {name} is on cuda:{x.device.index}, but the current device "
-                         f"(where the kernels run) is cuda:{_current_device()}")
+    if cuda:
+        cur = dev[0] if dev is not None else None
+        if cur is None:
+            cur = _current_device()
+            if dev is not None:
+                dev[0] = cur
+        if x.device.index != cur:
+            raise ValueError(f"{where}: {name} is on cuda:{x.device.index}, but the current device "
+                             f"(where the kernels run) is cuda:{cur}")
     return x.data_ptr()
 
 
 def _ring_args(desc, q, k, v, o, m, l, where: str, cuda: bool = True):
     import torch
     b, S, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
-    return (_arg(q, "q", where, torch.bfloat16, b * S * hq * d, cuda=cuda),
-            _arg(k, "k", where, torch.bfloat16, b * S * hkv * d, cuda=cuda),
-            _arg(v, "v", where, torch.bfloat16, b * S * hkv * d, cuda=cuda),
-            _arg(o, "o", where, torch.float32, b * S * hq * d, cuda=cuda),
-            _arg(m, "m", where, torch.float32, b * hq * S, cuda=cuda),
-            _arg(l, "l", where, torch.float32, b * hq * S, cuda=cuda))
+    dev = [None]
+    return (_arg(q, "q", where, torch.bfloat16, b * S * hq * d, cuda=cuda, dev=dev),
+            _arg(k, "k", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
+            _arg(v, "v", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
+            _arg(o, "o", where, torch.float32, b * S * hq * d, cuda=cuda, dev=dev),
+            _arg(m, "m", where, torch.float32, b * hq * S, cuda=cuda, dev=dev),
+            _arg(l, "l", where, torch.float32, b * hq * S, cuda=cuda, dev=dev))
 
 
 def _merge_args(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out, where: str):
     import torch
     n, b, r, h, d = int(n_parts), int(batch), int(rows), int(heads), int(d)
-    return (_arg(o_parts, "o_parts", where, torch.float32, n * b * r * h * d),
-            _arg(m_parts, "m_parts", where, torch.float32, n * b * h * r),
-            _arg(l_parts, "l_parts", where, torch.float32, n * b * h * r),
-            _arg(o_out, "o_out", where, torch.float32, b * r * h * d),
-            _arg(m_out, "m_out", where, torch.float32, b * h * r),
-            _arg(l_out, "l_out", where, torch.float32, b * h * r))
+    dev = [None]
+    return (_arg(o_parts, "o_parts", where, torch.float32, n * b * r * h * d, dev=dev),
+            _arg(m_parts, "m_parts", where, torch.float32, n * b * h * r, dev=dev),
+            _arg(l_parts, "l_parts", where, torch.float32, n * b * h * r, dev=dev),
+            _arg(o_out, "o_out", where, torch.float32, b * r * h * d, dev=dev),
+            _arg(m_out, "m_out", where, torch.float32, b * h * r, dev=dev),
+            _arg(l_out, "l_out", where, torch.float32, b * h * r, dev=dev))
 
 
 def _decode_args(desc, q, k, v, out, m_out, l_out, where: str):
     import torch
     b, L, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
-    return (_arg(q, "q", where, torch.bfloat16, b * hq * d),
-            _arg(k, "k", where, torch.bfloat16, b * L * hkv * d),
-            _arg(v, "v", where, torch.bfloat16, b * L * hkv * d),
-            _arg(out, "out", where, torch.float32, b * hq * d),
-            _arg(m_out, "m_out", where, torch.float32, b * hq),
-            _arg(l_out, "l_out", where, torch.float32, b * hq))
+    dev = [None]
+    return (_arg(q, "q", where, torch.bfloat16, b * hq * d, dev=dev),
+            _arg(k, "k", where, torch.bfloat16, b * L * hkv * d, dev=dev),
+            _arg(v, "v", where, torch.bfloat16, b * L * hkv * d, dev=dev),
+            _arg(out, "out", where, torch.float32, b * hq * d, dev=dev),
+            _arg(m_out, "m_out", where, torch.float32, b * hq, dev=dev),
+            _arg(l_out, "l_out", where, torch.float32, b * hq, dev=dev))
 
 
 def _stream(stream) -> Optional[int]:

@@ -26,8 +26,8 @@ cudaError_t cpattn::current_sm_count(int* sms) {
 }
 
 namespace {
-constexpr int kKnobs = 2;
-std::atomic<int32_t> g_kernel_choice[kKnobs] = {{-1}, {-1}};
+constexpr int kKnobs = 3;
+std::atomic<int32_t> g_kernel_choice[kKnobs] = {{-1}, {-1}, {-1}};
 }  // namespace
 
 int32_t cpattn::kernel_choice(int32_t knob) {
@@ -433,7 +433,8 @@ cp_status cp_ring_attn_host(const cp_attn_desc* desc, const void* q_host, const 
     chk(cudaStreamWaitEvent(cs, e_q(u), 0));
     if (!ok) break;
     st = launch_ring_attn(d, CP_LAYOUT_BALANCED, r0, r1, 0, cp, dq, dk, dv, dout, dm, dl,
-                          CP_MODE_EMIT | CP_MODE_FINALIZE, cs, u < n_half ? kRingFirstChunk : kRingSecondChunk);
+                          CP_MODE_EMIT | CP_MODE_FINALIZE, cs, u < n_half ? kRingFirstChunk : kRingSecondChunk,
+                          false);
     if (st != CP_OK) {
       ok = false;
       break;

@@ -68,10 +68,13 @@ bool ring_supported(const cp_attn_desc& d);
 // Returns CP_OK, or CP_ERR_CUDA when a tensor map cannot be encoded or the launch fails.
 // Which of each selected rank's two chunks a ring launch computes.
 enum RingChunks : int32_t { kRingBothChunks = 0, kRingFirstChunk = 1, kRingSecondChunk = 2 };
+// allow_split: a launch of few single query tiles may split their key walks over CTA
+// clusters (results equal within rounding); the host-buffer ring's partial launches do
+// not, so that they compute exactly what the one device launch would without the split.
 cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_begin, int32_t rank_end,
                            int32_t step_begin, int32_t step_end, const void* q, const void* k,
                            const void* v, float* o, float* m, float* l, int32_t mode,
-                           cudaStream_t stream, int32_t chunks = kRingBothChunks);
+                           cudaStream_t stream, int32_t chunks = kRingBothChunks, bool allow_split = true);
 // Reads and clears the ring kernel's device status word (after the caller synchronised).
 cudaError_t ring_take_status(int32_t* status);
 // Launches one CTA whose bounded wait can never complete (records CP_ERR_TIMEOUT).

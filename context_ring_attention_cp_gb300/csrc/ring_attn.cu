@@ -88,6 +88,10 @@ struct Cfg {
   static constexpr int kKvOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKvOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 1024 + 1024;  // barriers/flags + alignment slack
+  // A launch whose key walks are split over a cluster also exchanges each row's (m, l)
+  // and the merge weights through shared memory after the barriers.
+  static constexpr int kSplitOff = kBarOff + 1024;
+  static constexpr int kSplitSmemBytes = kSmemBytes + 2048;
   static constexpr uint32_t kOCol = 256;
 };
 
@@ -114,6 +118,7 @@ struct RingParams {
   int32_t chunks;                // RingChunks: both chunks of each rank, or only the first / second
   int32_t unit_groups;           // (sequence, kv head) units are taken in this many groups
   float sl;           // scale * log2(e)
+  int32_t kv_split;   // CTAs (one cluster) that share each item's key walk; 1 = not split
 };
 
 // ---------------------------------------------------------------------------
@@ -221,7 +226,7 @@ struct Item {
 };
 
 template <int LAYOUT>
-__device__ __forceinline__ Item decode_item(const RingParams& p) {
+__device__ __forceinline__ Item decode_item(const RingParams& p, int32_t item) {
   Item it;
   const int32_t nr = p.rank_end - p.rank_begin;
   const int32_t n_qt = (p.chunks == kRingBothChunks ? 2 : 1) * nr * p.ipc;  // row items of the selected chunks
@@ -231,8 +236,8 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
   const int32_t upg = int32_t(p.b * p.h_kv) / p.unit_groups;  // units per group
   const int32_t per_tile = upg * p.ppg;
   const int32_t per_group = n_qt * per_tile;
-  const int32_t g = int32_t(blockIdx.x) / per_group;
-  const int32_t idx = int32_t(blockIdx.x) - g * per_group;
+  const int32_t g = item / per_group;
+  const int32_t idx = item - g * per_group;
   const int32_t gq = n_qt - 1 - idx / per_tile;
   const int32_t bp = idx - (n_qt - 1 - gq) * per_tile;
   const int32_t u = bp / p.ppg;
@@ -279,7 +284,129 @@ __device__ __forceinline__ Item decode_item(const RingParams& p) {
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <int D, int LAYOUT>
+// Cluster-wide barrier of all threads: arrive with release semantics (this CTA's
+// shared-memory writes become visible to the cluster), wait with acquire semantics.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr) : "memory");
+  return v;
+}
+
+// The merge of a split item, run by the 128 threads of warps 4-7 of cluster CTA `part`
+// after the first cluster barrier: rows [part * R, (part + 1) * R) of the tile, R = 128 /
+// kv_split.  Per row: m = max over the parts, part weights w = e^{m_part - m} (0 for a
+// part that saw no key), l = sum of w * l_part in part order; then O = sum of w * O_part
+// in part order, and the launch's mode (EMIT / ACCUMULATE, FINALIZE) as in the
+// unsplit epilogue.
+template <int D>
+__device__ __noinline__ void split_merge(const RingParams& p, const Item& it, int32_t part, uint8_t* smem,
+                                         uint32_t sbase) {
+  using K = Cfg<D>;
+  const int P = p.kv_split;
+  const int R = BM / P;
+  const int t = threadIdx.x - 128;
+  float* xm = reinterpret_cast<float*>(smem + K::kSplitOff);
+  float* wt = xm + 2 * BM;       // [R][P] part weights
+  float* wo = wt + BM;           // [R] weight of the merged O (new part)
+  float* wold = wo + R;          // [R] weight of the O already in memory (ACCUMULATE)
+  const uint32_t xm_a = smem_u32(xm);
+  const uint32_t stage = sbase + uint32_t(K::kQOff);
+  const bool accumulate = (p.mode & CP_MODE_ACCUMULATE) != 0;
+  const bool fin = (p.mode & CP_MODE_FINALIZE) != 0;
+  if (t < R) {
+    const int r = part * R + t;  // row within the tile
+    const int32_t row = it.q_row0 + r;
+    float mx = -INFINITY;
+    for (int q = 0; q < P; ++q) mx = fmaxf(mx, ld_cluster_f32(cluster_addr(xm_a + uint32_t(r * 4), uint32_t(q))));
+    const float sh = (mx == -INFINITY) ? 0.f : mx;
+    float l = 0.f;
+    for (int q = 0; q < P; ++q) {
+      const float mq = ld_cluster_f32(cluster_addr(xm_a + uint32_t(r * 4), uint32_t(q)));
+      const float lq = ld_cluster_f32(cluster_addr(xm_a + uint32_t((BM + r) * 4), uint32_t(q)));
+      const float w = __expf(mq - sh);
+      wt[t * P + q] = w;
+      l = fmaf(w, lq, l);
+    }
+    // The merged triple (mx, l, O) against the mode, as the unsplit epilogue does.
+    float alpha = 0.f, beta = 1.f, l_out = l, m_out = mx;
+    const bool row_ok = r < it.q_rows && row < p.S;
+    const int64_t ml_off = (int64_t(it.bi) * p.h_q + it.h0) * p.S + row;
+    if (accumulate && row_ok) {
+      const float m_old = p.m[ml_off];
+      const float l_old = p.l[ml_off];
+      m_out = fmaxf(m_old, mx);
+      const float s2 = (m_out == -INFINITY) ? 0.f : m_out;
+      alpha = __expf(m_old - s2);
+      beta = __expf(mx - s2);
+      l_out = alpha * l_old + beta * l;
+    }
+    const float inv = (fin && l_out > 0.f) ? 1.f / l_out : (fin ? 0.f : 1.f);
+    wo[t] = beta * inv;
+    wold[t] = alpha * inv;
+    if (row_ok) {
+      p.m[ml_off] = m_out;
+      p.l[ml_off] = l_out;
+    }
+  }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  constexpr int kVec = D / 4;  // float4 columns of a row
+  for (int e = t; e < R * kVec; e += 128) {
+    const int rl = e / kVec, c4 = e - rl * kVec;
+    const int r = part * R + rl;
+    const int32_t row = it.q_row0 + r;
+    // box c4 / 8, row r, 16-byte chunk (c4 % 8) at position (c4 % 8) ^ (r % 8)
+    const uint32_t off = stage + uint32_t((c4 / 8) * BM * 128 + r * 128 + (((c4 % 8) ^ (r & 7)) << 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < P; ++q) {
+      const float w = wt[rl * P + q];
+      const float4 x = ld_cluster_v4(cluster_addr(off, uint32_t(q)));
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
+    }
+    if (r < it.q_rows && row < p.S) {
+      float4* dst = reinterpret_cast<float4*>(p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + it.h0) * D) + c4;
+      const float wn = wo[rl];
+      float4 v;
+      if (accumulate) {
+        const float4 old = *dst;
+        const float wd = wold[rl];
+        v = make_float4(fmaf(old.x, wd, acc.x * wn), fmaf(old.y, wd, acc.y * wn), fmaf(old.z, wd, acc.z * wn),
+                        fmaf(old.w, wd, acc.w * wn));
+      } else {
+        v = make_float4(acc.x * wn, acc.y * wn, acc.z * wn, acc.w * wn);
+      }
+      *dst = v;
+    }
+  }
+}
+
+// SPLIT: the CTAs of a cluster of p.kv_split share one item (one query tile): each walks a
+// contiguous part of its K/V tiles, stages its partial triple in shared memory, and after
+// a cluster barrier each merges a slice of the tile's rows from every part through
+// distributed shared memory (the associative merge of the Terms table's "Partial
+// attention" row) and writes them.  Used for launches of single query tiles that fill
+// less than half the GPU, which otherwise run as one CTA's chain of K/V tiles.
+template <int D, int LAYOUT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_constant__ RingParams p) {
   using K = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -301,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const Item it = decode_item<LAYOUT>(p);
+  const int32_t part = SPLIT ? int32_t(blockIdx.x) % p.kv_split : 0;  // this CTA's rank in its cluster
+  const Item it = decode_item<LAYOUT>(p, SPLIT ? int32_t(blockIdx.x) / p.kv_split : int32_t(blockIdx.x));
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -329,9 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
-  // Number of KV tiles this query tile visits over the step range.
-  const int32_t n_kv = KvCursor<LAYOUT>::count(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C,
-                                               it.q_last);
+  // Number of KV tiles this query tile visits over the step range; split, this CTA's
+  // contiguous part of them, from tile kv_lo on.
+  const int32_t n_all = KvCursor<LAYOUT>::count(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C,
+                                                it.q_last);
+  const int32_t kv_lo = SPLIT ? part * n_all / p.kv_split : 0;
+  const int32_t n_kv = SPLIT ? (part + 1) * n_all / p.kv_split - kv_lo : n_all;
   const int n_q = 1 + it.has_b;
 
   // Register split (launched with 168 per thread, 64,512 in all): the producer /
@@ -357,6 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last);
       int32_t key0, key_end;
       bool diag;
+      if constexpr (SPLIT)
+        for (int32_t i = 0; i < kv_lo; ++i) cur.next(key0, key_end, diag);
       int32_t li = 0;  // load index: K_j = 2j, V_j = 2j + 1
       bool ok = true;
       // ACCUMULATE reads the running triple at the end: bring its O tiles and m, l rows
@@ -379,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         }
         prefetched = true;
       };
-      while (ok && cur.next(key0, key_end, diag)) {
+      while (ok && (!SPLIT || li < 2 * n_kv) && cur.next(key0, key_end, diag)) {
         for (int which = 0; which < 2 && ok; ++which, ++li) {
           if (!prefetched && li == K::kStages) prefetch_old();
           const int s = li % K::kStages;
@@ -496,6 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
     KvCursor<LAYOUT> cur;
     cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last);
+    if constexpr (SPLIT) {
+      int32_t key0, key_end;
+      bool diag;
+      for (int32_t i = 0; i < kv_lo; ++i) cur.next(key0, key_end, diag);
+    }
     for (int32_t j = 0; j < n_kv; ++j) {
       int32_t key0 = 0, key_end = 0;
       bool diag = false;
@@ -591,6 +729,33 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const float fre = (m_true == -INFINITY) ? 0.f : ex2(m_ref - m_true);
       const float m_new_nat = m_true * kLn2;
       const float l_new = l_run * fre;
+      if constexpr (SPLIT) {
+        // This part's triple of every row of the tile, against the part's own max: m and
+        // l into the exchange arrays, O * 2^(m_ref - m_true) into the Q tiles' space
+        // (every MMA that read it has completed) in the 128-byte-swizzled layout of the
+        // staged stores.  The merge after the cluster barrier reads them.
+        float* xm = reinterpret_cast<float*>(smem + K::kSplitOff);
+        xm[t] = m_new_nat;
+        xm[BM + t] = l_new;
+        const uint32_t stage = sbase + uint32_t(K::kQOff);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          if (have) {
+            tmem_ld32(o_addr + uint32_t(c * 32), r);
+            tmem_ld_wait(r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          const uint32_t rowa = stage + uint32_t(c * BM * 128 + t * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_shared_v4(rowa + uint32_t(((k ^ (t & 7)) << 4)), __uint_as_float(r[4 * k]) * fre,
+                         __uint_as_float(r[4 * k + 1]) * fre, __uint_as_float(r[4 * k + 2]) * fre,
+                         __uint_as_float(r[4 * k + 3]) * fre);
+        }
+      } else {
       const bool row_ok = t < rows && row < p.S;
       const bool accumulate = (p.mode & CP_MODE_ACCUMULATE) != 0;
       // A whole 128-row tile moves its O rows through shared memory with TMA.
@@ -712,9 +877,20 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         p.m[ml_off] = m_out;
         p.l[ml_off] = l_out;
       }
+      }  // !SPLIT
     }
   }
 
+  }
+
+  if constexpr (SPLIT) {
+    // Every thread of every CTA of the cluster passes both barriers (no role returns
+    // early and every wait before them is bounded), so they always complete.  The first
+    // makes the parts' staged triples visible across the cluster; the second keeps each
+    // CTA's shared memory alive until every peer has read it.
+    cluster_sync_all();
+    if (warp >= 4 && warp < 8 && !skip) split_merge<D>(p, it, part, smem, sbase);
+    cluster_sync_all();
   }
 
   tc_fence_before();
@@ -777,10 +953,30 @@ bool encode_map(CUtensorMap* map, const void* base, int64_t b, int64_t S, int64_
 template <int D, int LAYOUT>
 cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
   using K = Cfg<D>;
-  if (cudaFuncSetAttribute(ring_attn_kernel<D, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (LAYOUT == CP_LAYOUT_BALANCED && p.kv_split > 1) {
+    // One cluster of kv_split CTAs per item (at most 8, the portable cluster size).
+    auto kern = ring_attn_kernel<D, CP_LAYOUT_BALANCED, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSplitSmemBytes) != cudaSuccess)
+      return CP_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(unsigned(n_items * p.kv_split), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = K::kSplitSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.kv_split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(ring_attn_kernel<D, LAYOUT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            K::kSmemBytes) != cudaSuccess)
     return CP_ERR_CUDA;
-  ring_attn_kernel<D, LAYOUT><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
+  ring_attn_kernel<D, LAYOUT, false><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }
 
@@ -793,7 +989,8 @@ bool ring_supported(const cp_attn_desc& d) {
 
 cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_begin, int32_t rank_end,
                            int32_t step_begin, int32_t step_end, const void* q, const void* k, const void* v,
-                           float* o, float* m, float* l, int32_t mode, cudaStream_t stream, int32_t chunks) {
+                           float* o, float* m, float* l, int32_t mode, cudaStream_t stream, int32_t chunks,
+                           bool allow_split) {
   RingParams p;
   memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tmap_q, q, d.b, d.S, d.h_q, d.d) || !encode_map(&p.tmap_k, k, d.b, d.S, d.h_kv, d.d) ||
@@ -857,6 +1054,16 @@ cp_status launch_ring_attn(const cp_attn_desc& d, int32_t layout, int32_t rank_b
   const int64_t n_items =
       int64_t(chunks == kRingBothChunks ? 2 : 1) * (rank_end - rank_begin) * p.ipc * d.b * p.n_pairs;
   if (n_items > 0x7fffffffLL) return CP_ERR_UNSUPPORTED;
+  // Single query tiles that fill at most half the GPU: each item's key walk is split over
+  // a cluster of 2, 4 or 8 CTAs (the most that still fit in one wave), which shortens the
+  // chain of K/V tiles each CTA runs.  CP_KNOB_RING_KV_SPLIT = 0 turns this off.
+  p.kv_split = 1;
+  if (allow_split && layout == CP_LAYOUT_BALANCED && !p.row_pairs && p.group == 1 &&
+      kernel_choice(CP_KNOB_RING_KV_SPLIT) != 0) {
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return CP_ERR_CUDA;
+    while (p.kv_split < 8 && n_items * p.kv_split * 2 <= int64_t(sms)) p.kv_split *= 2;
+  }
   if (layout == CP_LAYOUT_SEQUENTIAL)
     return d.d == 128 ? launch_d<128, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream)
                       : launch_d<64, CP_LAYOUT_SEQUENTIAL>(p, n_items, stream);

@@ -129,7 +129,10 @@ CPATTN_API cp_status cp_plan_chunks(int64_t S, int32_t cp, int32_t layout, int64
  * heads of one kv group (even h_q / h_kv) or two consecutive row tiles of one head
  * (odd).  With h_q == h_kv, a launch with at most one wave (SM count) of single tiles
  * keeps one tile per CTA; cp_set_kernel_choice(CP_KNOB_RING_PAIRING, ...) overrides
- * that choice, and every choice gives the same bits.
+ * that choice, and every choice gives the same bits.  When such single tiles fill at
+ * most half the GPU, each tile's key walk is split over a cluster of 2-8 CTAs whose
+ * partial triples are merged on chip (CP_KNOB_RING_KV_SPLIT); the result then equals
+ * the unsplit one within rounding.
  * Supported: d in {64, 128}; causal = 1; every pointer 16-byte aligned.
  * Errors: cp < 1, S % (2cp) != 0, h_q % h_kv != 0, any size < 1, scale <= 0 or
  * not finite, 0 <= step_begin < step_end <= cp violated, unknown mode bits, NULL or
@@ -336,17 +339,21 @@ CPATTN_API cp_status cp_comm_bytes(const cp_comm_query* query, cp_comm_result* r
 
 /*
  * Kernel-choice settings, for tests and diagnostics (the pages have no counterpart:
- * each knob picks between kernels of this library that compute the same bits).
+ * each knob picks between kernels of this library that compute the same result).
  *   CP_KNOB_RING_PAIRING  -1 automatic (default); 0 one query tile per CTA for
  *                         launches with h_q == h_kv; 1 two tiles per CTA always.
  *   CP_KNOB_MERGE_KERNEL  -1 automatic (default: TMA-fed where supported);
  *                         0 the plain-load kernel; 1 the same as -1.
+ *   CP_KNOB_RING_KV_SPLIT -1 automatic (default); 0 never split a query tile's key
+ *                         walk over a CTA cluster; 1 the same as -1.  The split
+ *                         merges the parts' triples in another order, so its results
+ *                         equal the unsplit ones within rounding, not bit for bit.
  * The setting is process-wide, applies to every device and to launches made after
  * the call returns, and is read once per launch (no environment variable is read
  * anywhere in the library).
  * Errors: an unknown knob or a value outside {-1, 0, 1} -> CP_ERR_INVALID_ARGUMENT.
  */
-enum { CP_KNOB_RING_PAIRING = 0, CP_KNOB_MERGE_KERNEL = 1 };
+enum { CP_KNOB_RING_PAIRING = 0, CP_KNOB_MERGE_KERNEL = 1, CP_KNOB_RING_KV_SPLIT = 2 };
 CPATTN_API cp_status cp_set_kernel_choice(int32_t knob, int32_t value);
 
 /*

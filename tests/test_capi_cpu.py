@@ -397,12 +397,12 @@ def test_binding_rejects_a_tensor_on_another_device(cpa, monkeypatch):
 
 def test_kernel_choice_settings(cpa):
     lib = cpa.load_library()
-    for knob in (cpa.CP_KNOB_RING_PAIRING, cpa.CP_KNOB_MERGE_KERNEL):
+    for knob in (cpa.CP_KNOB_RING_PAIRING, cpa.CP_KNOB_MERGE_KERNEL, cpa.CP_KNOB_RING_KV_SPLIT):
         for value in (-1, 0, 1, -1):
             cpa.cp_set_kernel_choice(knob, value)
         for bad in (-2, 2):
             assert lib.cp_set_kernel_choice(knob, bad) == 1
-    for bad_knob in (-1, 2, 99):
+    for bad_knob in (-1, 3, 99):
         with pytest.raises(cpa.CpError) as e:
             cpa.cp_set_kernel_choice(bad_knob, 0)
         assert e.value.status == 1

@@ -3,7 +3,9 @@
 cp_ring_attn_host runs the same kernel over groups of virtual ranks, with the
 copies in and out overlapped, so its outputs must equal cp_ring_step_partial_attn
 over all steps in EMIT | FINALIZE mode bit for bit (each CTA computes the same
-rows from the same data in either launch).  One case is also held to the fp64
+rows from the same data in either launch).  Its partial launches never split a
+query tile's key walk over a CTA cluster, so the device launch it is compared
+with runs with that split turned off.  One case is also held to the fp64
 oracle at the suite's prefill tolerances (output max-abs <= 2e-2, mean-abs <=
 2e-3; lse within 2e-3).
 """
@@ -41,6 +43,9 @@ def _lib():
     from context_ring_attention_cp_gb300 import _build
     _build.build()
     cpa.load_library()
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, 0)
+    yield
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
 
 
 def _host_call(desc, q, k, v, pinned=True):

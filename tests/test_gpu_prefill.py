@@ -472,6 +472,7 @@ def test_tile_pairing_modes_give_the_same_bits(case):
     b, S, hq, hkv, d, cp, std = case
     q, k, v = _inputs(b, S, hq, hkv, d, std, seed=11)
     got = {}
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, 0)  # the split sums in another order
     try:
         for mode in ("single", "pair", "auto"):
             cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, {"single": 0, "pair": 1, "auto": -1}[mode])
@@ -483,7 +484,76 @@ def test_tile_pairing_modes_give_the_same_bits(case):
             got[mode] = (full, step, acc)
     finally:
         cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)  # this module's setting
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
     for mode in ("pair", "auto"):
         for xs, ys in zip(got["single"], got[mode]):
             for x, y in zip(xs, ys):
                 assert torch.equal(x, y), f"{mode} {case}"
+
+
+# Single query tiles filling at most half the GPU split each tile's key walk over a
+# cluster of 2, 4 or 8 CTAs and merge the parts' triples on chip.  (b, S, h_q, h_kv, d,
+# cp, std): the tiny workload (32 tiles, clusters of 4), ragged 122-row tiles, chunks
+# shorter than a tile, cp = 1, one-token chunks (parts that see no key), 64 tiles
+# (clusters of 2), b = 2.
+SPLIT = [
+    (1, 1024, 4, 4, 64, 2, 1.0),
+    (1, 1000, 2, 2, 128, 2, 1.0),
+    (2, 768, 3, 3, 64, 4, 1.0),
+    (1, 384, 3, 3, 64, 1, 1.0),
+    (1, 8, 2, 2, 64, 4, 1.0),
+    (1, 4096, 2, 2, 128, 4, 0.5),
+    (1, 2048, 1, 1, 128, 8, 0.5),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT, ids=[str(c) for c in SPLIT])
+def test_key_walk_split_over_a_cluster(case):
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=500 + (hash(case) & 0xFF))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    scale = 1.0 / math.sqrt(d)
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 0)  # one query tile per CTA: the split's form
+    try:
+        # the whole ring against the oracle, and against the unsplit launch
+        o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        ref_out, ref_m, ref_l, _ = OA.full_causal_attention(qf, kf, vf, scale)
+        assert_out_close(o.cpu().numpy(), ref_out, f"split {case}")
+        assert np.abs(m.cpu().numpy() - ref_m).max() <= LSE_ABS
+        assert np.abs((m + torch.log(l)).cpu().numpy() - (ref_m + np.log(ref_l))).max() <= LSE_ABS
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, 0)
+        uo, um, ul = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
+        assert torch.equal(m, um)  # the max is exact in any grouping
+        # P is rounded to bf16 against each part's own exponent reference (as between two
+        # step-range launches), so the outputs agree at that rounding level
+        assert (o - uo).abs().max().item() <= 5e-3
+        assert ((l - ul).abs() <= 1e-5 * ul.abs()).all()
+        # every step's triple against the oracle's step triple (identity rows exact)
+        for t in range(cp):
+            so, sm, sl = run_ring(q, k, v, cp, t, t + 1, EMIT)
+            so, sm, sl = so.cpu().numpy(), sm.cpu().numpy(), sl.cpu().numpy()
+            for r in range(cp):
+                rows, rm, rl, ro = OR.ring_step_triple(qf, kf, vf, scale, cp, r, t)
+                gm, gl = sm[:, :, rows], sl[:, :, rows]
+                go = np.moveaxis(so[:, rows], 1, 2)
+                empty = np.isneginf(rm)
+                assert np.all(np.isneginf(gm[empty])) and np.all(gl[empty] == 0) and np.all(go[empty] == 0)
+                live = ~empty
+                assert np.abs(gm[live] - rm[live]).max(initial=0.0) <= LSE_ABS
+                if live.any():
+                    assert_out_close(go[live] / gl[live][:, None], ro[live] / rl[live][:, None],
+                                     f"split step {t} rank {r}")
+        # the steps accumulated in reverse order, then finalised
+        bufs = ring_buffers(b, S, hq, d, identity=True)
+        for i, t in enumerate(range(cp)[::-1]):
+            run_ring(q, k, v, cp, t, t + 1, ACC | (FIN if i == cp - 1 else 0), bufs)
+        assert_out_close(bufs[0].cpu().numpy(), ref_out, f"split accumulated {case}")
+        # ACCUMULATE into the identity triple stores what EMIT stores, bit for bit
+        acc = run_ring(q, k, v, cp, 0, 1, ACC, ring_buffers(b, S, hq, d, identity=True))
+        emit = run_ring(q, k, v, cp, 0, 1, EMIT)
+        for x, y in zip(acc, emit):
+            assert torch.equal(x, y)
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)  # this module's setting
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
