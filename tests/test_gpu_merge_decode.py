@@ -173,11 +173,29 @@ def test_tree_merge_rejects_bad_part_counts():
         cpa.cp_merge_partials_tree(1, 8, 2, 8, 3, o, m, l, ws, ws.numel() * 4, out, ml, ml.clone())
 
 
-@pytest.mark.parametrize("shape", [(2, 2, 33, 3, 64), (8, 2, 33, 3, 64), (32, 1, 64, 4, 128), (64, 2, 20, 3, 32),
-                                   (128, 1, 24, 2, 64), (256, 1, 16, 2, 16)])
-def test_tree_merge_equals_level_by_level_two_part_merges(shape):
+TREE_LEVEL_SHAPES = [(2, 2, 33, 3, 64), (8, 2, 33, 3, 64), (32, 1, 64, 4, 128), (64, 2, 20, 3, 32),
+                     (128, 1, 24, 2, 64), (256, 1, 16, 2, 16),
+                     # d = 128 with up to 64 parts: the TMA-fed kernels (ragged 16-row blocks, b > 1)
+                     (2, 2, 33, 3, 128), (4, 1, 16, 1, 128), (8, 3, 40, 2, 128), (16, 1, 7, 5, 128),
+                     (64, 2, 20, 3, 128)]
+
+
+@pytest.mark.parametrize("kernel", [-1, 0], ids=["auto", "plain-load"])
+@pytest.mark.parametrize("shape", TREE_LEVEL_SHAPES)
+def test_tree_merge_equals_level_by_level_two_part_merges(shape, kernel):
     # The one-pass tree does at every node what a two-part merge does, so it must
-    # equal the halving tree run level by level through cp_merge_partials bit for bit.
+    # equal the halving tree run level by level through cp_merge_partials bit for bit,
+    # with the TMA-fed kernels (d = 128, up to 64 parts) and with the plain-load ones.
+    if kernel == 0 and shape[-1] != 128:
+        pytest.skip("only d = 128 has a second kernel")
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_MERGE_KERNEL, kernel)
+    try:
+        _tree_vs_levels(shape)
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_MERGE_KERNEL, -1)
+
+
+def _tree_vs_levels(shape):
     n, b, rows, heads, d = shape
     draws = [synth.merge_parts(n, heads, rows, d, spread=80.0, seed=11 * n + bi) for bi in range(b)]
     o = torch.cat([x[0] for x in draws], dim=1).contiguous()
