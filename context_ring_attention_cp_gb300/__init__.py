@@ -154,7 +154,8 @@ def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, 
         raise ValueError(f"{where}: {name} holds {n} elements, the descriptor needs {numel}")
     if nbytes and n * x.element_size() < nbytes:
         raise ValueError(f"{where}: {name} holds {n * x.element_size()} bytes, {nbytes} were passed")
-    if x.is_cuda != cuda:
+    index = x.get_device()  # -1 for a host tensor
+    if (index >= 0) != cuda:
         raise ValueError(f"{where}: {name} must be a {'CUDA' if cuda else 'host (CPU)'} tensor")
     if cuda:
         cur = dev[0] if dev is not None else None
@@ -162,16 +163,16 @@ def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, 
             cur = _current_device()
             if dev is not None:
                 dev[0] = cur
-        if x.device.index != cur:
-            raise ValueError(f"{where}: {name} is on cuda:{x.device.index}, but the current device "
+        if index != cur:
+            raise ValueError(f"{where}: {name} is on cuda:{index}, but the current device "
                              f"(where the kernels run) is cuda:{cur}")
     return x.data_ptr()
 
 
-def _ring_args(desc, q, k, v, o, m, l, where: str, cuda: bool = True):
+def _ring_args(desc, q, k, v, o, m, l, where: str, cuda: bool = True, dev: Optional[list] = None):
     import torch
     b, S, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
-    dev = [None]
+    dev = [None] if dev is None else dev
     return (_arg(q, "q", where, torch.bfloat16, b * S * hq * d, cuda=cuda, dev=dev),
             _arg(k, "k", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
             _arg(v, "v", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
@@ -204,10 +205,16 @@ def _decode_args(desc, q, k, v, out, m_out, l_out, where: str):
             _arg(l_out, "l_out", where, torch.float32, b * hq, dev=dev))
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, dev: Optional[list] = None) -> Optional[int]:
+    """The cudaStream_t to launch on: the given stream, or the current stream of the current
+    device (``dev`` may hold that device, looked up by the argument checks)."""
     if stream is None:
         import torch
-        return torch.cuda.current_stream().cuda_stream
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is None:
+            return torch.cuda.current_stream().cuda_stream
+        d = dev[0] if dev is not None and dev[0] is not None else torch.cuda.current_device()
+        return raw(d)
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -267,9 +274,10 @@ def cp_ring_step_partial_attn(desc: AttnDesc, step_begin: int, step_end: int, q,
                               mode: int = CP_MODE_EMIT, stream=None) -> None:
     """Ring steps [step_begin, step_end) for all virtual ranks (see include/cpattn.h)."""
     lib = load_library()
-    ptrs = _ring_args(desc, q, k, v, o, m, l, "cp_ring_step_partial_attn")
+    dev = [None]
+    ptrs = _ring_args(desc, q, k, v, o, m, l, "cp_ring_step_partial_attn", dev=dev)
     st = lib.cp_ring_step_partial_attn(ctypes.byref(desc), int(step_begin), int(step_end), *ptrs, int(mode),
-                                       _stream(stream))
+                                       _stream(stream, dev))
     _check(st, "cp_ring_step_partial_attn")
 
 

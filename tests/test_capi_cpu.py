@@ -381,6 +381,9 @@ class _FakeCudaTensor:
     def data_ptr(self):
         return 4096
 
+    def get_device(self):
+        return self.device.index
+
 
 def test_binding_rejects_a_tensor_on_another_device(cpa, monkeypatch):
     # kernels run on the current device: a tensor of another GPU must never reach them
