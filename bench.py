@@ -624,6 +624,24 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                           "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
+    # head dimension 64 at scale: b1, 16/16 heads, d64, S32768, cp8 (half the MMA cycles of
+    # d128 for the same softmax work)
+    w = synth.WORKLOADS["mha64"]
+    q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+    o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+    m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+    l = torch.empty_like(m)
+    desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, stream)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = _events_time(fn, 10, stream)
+    tf = prefill_flops(w) / (ms * 1e-3) / 1e12
+    out["prefill_d64"] = {"workload": "prefill ring attention, head dimension 64: b1, 16/16 heads, d64, S32768, cp8",
+                          "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 3), "flops": prefill_flops(w),
+                          "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+    del q, k, v, o, m, l
+    torch.cuda.empty_cache()
     # tiny prefill: b1, 4/4 heads, d64, S1024, cp2 (0.54 GFLOP).  A few CTAs per head and
     # 1 MB of inputs that stay in L2: launch- and latency-bound, reported as measured.
     w = synth.WORKLOADS["tiny"]

@@ -36,6 +36,8 @@ WORKLOADS = {
     "merge": dict(kind="merge", heads=64, d=128, rows=4096, parts=32, spread=80.0, seed=20260005),
     # multi-head (one query head per K/V head) at the GQA workload's size
     "mha": dict(kind="prefill", b=1, S=32768, h_q=32, h_kv=32, d=128, cp=8, std=0.5, seed=20260006),
+    # head dimension 64 at scale: multi-head, 16 heads, the GQA workload's length and cp
+    "mha64": dict(kind="prefill", b=1, S=32768, h_q=16, h_kv=16, d=64, cp=8, std=0.5, seed=20260007),
 }
 
 _CHUNK = 1 << 26  # elements drawn per randn call (bounds the fp32 staging buffer)

@@ -299,7 +299,7 @@ def test_bounded_wait_timeout_is_reported_and_recovers():
     assert_out_close(o.cpu().numpy(), ref_out, "after recovery")
 
 
-@pytest.mark.parametrize("name", ["gqa", "long", "mha", "gqa-sequential"])
+@pytest.mark.parametrize("name", ["gqa", "long", "mha", "mha64", "gqa-sequential"])
 def test_full_size_workload_sampled_rows(name):
     """The benchmark's launch (all steps, one launch, finalised) at full size; rows sampled.
     gqa-sequential: the GQA workload under the sequential chunk layout, one launch per
