@@ -310,18 +310,19 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
   return v;
 }
 
-// The merge of a split item, run by the 128 threads of warps 4-7 of cluster CTA `part`
-// after the first cluster barrier: rows [part * R, (part + 1) * R) of the tile, R = 128 /
-// kv_split.  Per row: m = max over the parts, part weights w = e^{m_part - m} (0 for a
-// part that saw no key), l = sum of w * l_part in part order; then O = sum of w * O_part
-// in part order, and the launch's mode (EMIT / ACCUMULATE, FINALIZE) as in the
-// unsplit epilogue.
-template <int D>
+// The merge of a split item, run by the 256 threads of warps 4-11 of cluster CTA `part`
+// after the first cluster barrier: rows [part * R, (part + 1) * R) of the tile, R = 128 / P.  Per row: m =
+// max over the parts, part weights w = e^{m_part - m} (0 for a part that saw no key),
+// l = sum of w * l_part in part order; then O = sum of w * O_part in part order, and the
+// launch's mode (EMIT / ACCUMULATE, FINALIZE) as in the unsplit epilogue.  Every peer's
+// values are loaded before any is used, so the distributed shared-memory loads of a row
+// or a column block are in flight together.
+template <int D, int P>
 __device__ __noinline__ void split_merge(const RingParams& p, const Item& it, int32_t part, uint8_t* smem,
                                          uint32_t sbase) {
   using K = Cfg<D>;
-  const int P = p.kv_split;
-  const int R = BM / P;
+  constexpr int R = BM / P;
+  constexpr int kMergeThreads = 256;
   const int t = threadIdx.x - 128;
   float* xm = reinterpret_cast<float*>(smem + K::kSplitOff);
   float* wt = xm + 2 * BM;       // [R][P] part weights
@@ -334,16 +335,22 @@ __device__ __noinline__ void split_merge(const RingParams& p, const Item& it, in
   if (t < R) {
     const int r = part * R + t;  // row within the tile
     const int32_t row = it.q_row0 + r;
+    float mq[P], lq[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      mq[q] = ld_cluster_f32(cluster_addr(xm_a + uint32_t(r * 4), uint32_t(q)));
+      lq[q] = ld_cluster_f32(cluster_addr(xm_a + uint32_t((BM + r) * 4), uint32_t(q)));
+    }
     float mx = -INFINITY;
-    for (int q = 0; q < P; ++q) mx = fmaxf(mx, ld_cluster_f32(cluster_addr(xm_a + uint32_t(r * 4), uint32_t(q))));
+#pragma unroll
+    for (int q = 0; q < P; ++q) mx = fmaxf(mx, mq[q]);
     const float sh = (mx == -INFINITY) ? 0.f : mx;
     float l = 0.f;
+#pragma unroll
     for (int q = 0; q < P; ++q) {
-      const float mq = ld_cluster_f32(cluster_addr(xm_a + uint32_t(r * 4), uint32_t(q)));
-      const float lq = ld_cluster_f32(cluster_addr(xm_a + uint32_t((BM + r) * 4), uint32_t(q)));
-      const float w = __expf(mq - sh);
+      const float w = __expf(mq[q] - sh);
       wt[t * P + q] = w;
-      l = fmaf(w, lq, l);
+      l = fmaf(w, lq[q], l);
     }
     // The merged triple (mx, l, O) against the mode, as the unsplit epilogue does.
     float alpha = 0.f, beta = 1.f, l_out = l, m_out = mx;
@@ -366,22 +373,25 @@ __device__ __noinline__ void split_merge(const RingParams& p, const Item& it, in
       p.l[ml_off] = l_out;
     }
   }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");  // warps 4-11
   constexpr int kVec = D / 4;  // float4 columns of a row
-  for (int e = t; e < R * kVec; e += 128) {
+  for (int e = t; e < R * kVec; e += kMergeThreads) {
     const int rl = e / kVec, c4 = e - rl * kVec;
     const int r = part * R + rl;
     const int32_t row = it.q_row0 + r;
     // box c4 / 8, row r, 16-byte chunk (c4 % 8) at position (c4 % 8) ^ (r % 8)
     const uint32_t off = stage + uint32_t((c4 / 8) * BM * 128 + r * 128 + (((c4 % 8) ^ (r & 7)) << 4));
+    float4 x[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) x[q] = ld_cluster_v4(cluster_addr(off, uint32_t(q)));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
     for (int q = 0; q < P; ++q) {
       const float w = wt[rl * P + q];
-      const float4 x = ld_cluster_v4(cluster_addr(off, uint32_t(q)));
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+      acc.x = fmaf(w, x[q].x, acc.x);
+      acc.y = fmaf(w, x[q].y, acc.y);
+      acc.z = fmaf(w, x[q].z, acc.z);
+      acc.w = fmaf(w, x[q].w, acc.w);
     }
     if (r < it.q_rows && row < p.S) {
       float4* dst = reinterpret_cast<float4*>(p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + it.h0) * D) + c4;
@@ -469,8 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   // MMA warpgroup gives registers to the two softmax warpgroups.
   // 128 x 72 + 256 x 216 = 64,512 <= 64,512, so the increase never waits.  Each
   // role's code is reachable only after its own setmaxnreg; the common tail is tiny.
+  // A split launch's cluster barriers: every thread of every CTA of the cluster passes
+  // exactly two, in whichever branch below it takes (no role returns early and every wait
+  // before them is bounded), so they always complete.  The first makes the parts' staged
+  // triples visible across the cluster; the second keeps each CTA's shared memory alive
+  // until every peer has read it.  The merge between them runs in the softmax warps.
   if (skip) {
     // nothing to do: fall through to the teardown
+    if constexpr (SPLIT) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
   } else if (warp < 4) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
   if (warp == 0) {
@@ -608,6 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         }
       }
     }
+  }
+  if constexpr (SPLIT) {
+    cluster_sync_all();
+    cluster_sync_all();
   }
   } else {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
@@ -880,17 +903,18 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       }  // !SPLIT
     }
   }
-
+  if constexpr (SPLIT) {
+    // warps 4-11 (all 256 of them, whether or not they had a tile) merge the rows
+    cluster_sync_all();
+    if (p.kv_split == 2)
+      split_merge<D, 2>(p, it, part, smem, sbase);
+    else if (p.kv_split == 4)
+      split_merge<D, 4>(p, it, part, smem, sbase);
+    else
+      split_merge<D, 8>(p, it, part, smem, sbase);
+    cluster_sync_all();
   }
 
-  if constexpr (SPLIT) {
-    // Every thread of every CTA of the cluster passes both barriers (no role returns
-    // early and every wait before them is bounded), so they always complete.  The first
-    // makes the parts' staged triples visible across the cluster; the second keeps each
-    // CTA's shared memory alive until every peer has read it.
-    cluster_sync_all();
-    if (warp >= 4 && warp < 8 && !skip) split_merge<D>(p, it, part, smem, sbase);
-    cluster_sync_all();
   }
 
   tc_fence_before();
