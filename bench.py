@@ -76,7 +76,7 @@ def merge_bytes(w):
 # ring kernel on this workload, from the ncu capture of that kernel.  It is reported
 # only while ring_attn.cu is the source that was captured (sha256 prefix below);
 # otherwise traffic is null.
-RING_TRAFFIC = {"sha256_prefix": "c9d394c7b0694ff1", "bytes": 893814272}
+RING_TRAFFIC = {"sha256_prefix": "096e710071e8200f", "bytes": 893790208}
 
 
 def ring_traffic():
@@ -825,6 +825,17 @@ def profile_case(name, steps):
         fn = lambda: cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, stream)  # noqa: E731
         work = prefill_flops(w) / 1e3
         unit = "TFLOP/s"
+    elif name in ("ring-tiny", "ring-d64"):  # the tiny workload (key walks split over clusters) / d64 at scale
+        w = synth.WORKLOADS["tiny" if name == "ring-tiny" else "mha64"]
+        q, k, v = synth.prefill_inputs(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], std=w["std"], seed=w["seed"])
+        o = torch.empty((w["b"], w["S"], w["h_q"], w["d"]), dtype=torch.float32, device="cuda")
+        m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
+        l = torch.empty_like(m)
+        desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
+        mode = cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE
+        fn = lambda: cpa.cp_ring_step_partial_attn(desc, 0, w["cp"], q, k, v, o, m, l, mode, stream)  # noqa: E731
+        work = prefill_flops(w) / 1e3
+        unit = "TFLOP/s"
     elif name == "decode-small":  # b8, 16 heads, d512, L8192, cp8: 2.1 GB of K/V
         b, L, h, d, cp = 8, 8192, 16, 512, 8
         q, k, v = synth.decode_inputs(b, L, h, h, d, seed=7)
@@ -882,7 +893,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--case", choices=["ring-step", "ring-step-accumulate", "ring-mha", "decode-small",
+    ap.add_argument("--case", choices=["ring-step", "ring-step-accumulate", "ring-mha", "ring-tiny", "ring-d64",
+                                       "decode-small",
                                        "decode-shared-kv", "merge", "merge-tree"], default=None,
                     help="time one kernel on a capture-sized case (for ncu) instead of the benchmark")
     args = ap.parse_args()
