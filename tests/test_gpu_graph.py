@@ -95,6 +95,33 @@ def test_fused_ring_replays_bit_equal():
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("shape", [(1, 1024, 4, 4, 64, 2), (1, 1000, 2, 2, 128, 2)], ids=["tiny", "ragged_d128"])
+def test_split_ring_replays_bit_equal(shape):
+    # Few single query tiles: each tile's key walk is split over a cluster of CTAs (a
+    # cluster launch), which replays from a graph with the eager call's bits.
+    b, S, hq, hkv, d, cp = shape
+    q, k, v = synth.prefill_inputs(b, S, hq, hkv, d, std=1.0, seed=94)
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+    mode = cpa.CP_MODE_EMIT | cpa.CP_MODE_FINALIZE
+    outs = []
+    for graphed in (False, True):
+        o = torch.full((b, S, hq, d), float("nan"), dtype=torch.float32, device="cuda")
+        m = torch.full((b, hq, S), float("nan"), dtype=torch.float32, device="cuda")
+        l = torch.full_like(m, float("nan"))
+        fn = lambda st: cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, o, m, l, mode, st)  # noqa: E731
+        if graphed:
+            side = torch.cuda.Stream()
+            _replay(_capture(fn, side), side)
+        else:
+            fn(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+        assert cpa.cp_take_device_status() == 0
+        assert torch.isfinite(o).all()
+        outs.append((o, m, l))
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+
+
 def test_merge_and_tree_replay_bit_equal():
     n, b, rows, heads, d = 8, 1, 300, 3, 128
     gen = torch.Generator(device="cpu").manual_seed(93)

@@ -557,3 +557,60 @@ def test_key_walk_split_over_a_cluster(case):
     finally:
         cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)  # this module's setting
         cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
+
+
+def test_split_rank_launches_write_their_rows_and_compose():
+    # One launch per virtual rank (balanced layout) has few single tiles, so each splits its
+    # key walks over larger clusters than the all-ranks launch: every rank writes exactly
+    # its own rows, and together they give the oracle's attention.
+    b, S, hq, hkv, d, cp, std = 1, 2048, 2, 2, 64, 4, 1.0
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=77)
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 0)
+    try:
+        bufs = ring_buffers(b, S, hq, d)
+        for x in bufs:
+            x.fill_(float("nan"))
+        C = S // (2 * cp)
+        for r in range(cp):
+            _run_ranks(q, k, v, cp, cpa.CP_LAYOUT_BALANCED, r, r + 1, 0, cp, EMIT | FIN, bufs)
+            o = bufs[0].cpu().numpy()
+            own = np.zeros(S, bool)
+            for rr in range(r + 1):
+                own[rr * C:(rr + 1) * C] = True
+                own[(2 * cp - 1 - rr) * C:(2 * cp - rr) * C] = True
+            assert np.isfinite(o[0, own]).all() and np.isnan(o[0, ~own]).all(), f"rank {r}"
+        ref_out, ref_m, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+        assert_out_close(bufs[0].cpu().numpy(), ref_out, "split rank launches")
+        assert np.abs(bufs[1].cpu().numpy() - ref_m).max() <= LSE_ABS
+        full = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        assert torch.equal(full[1], bufs[1])  # the max is exact in any grouping
+        assert (full[0] - bufs[0]).abs().max().item() <= 5e-3
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)  # this module's setting
+
+
+def test_split_launch_skips_while_the_status_holds_an_error():
+    """A split launch (clusters of 4) queued behind a wait that gives up writes nothing and
+    completes: every CTA of every cluster passes both cluster barriers on the skip path."""
+    import time
+    assert cpa.cp_take_device_status() == 0
+    b, S, hq, hkv, d, cp = 1, 1024, 4, 4, 64, 2  # the tiny workload's shape
+    q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=42)
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 0)
+    try:
+        t0 = time.time()
+        cpa.cp_selftest_wait_timeout()
+        bufs = ring_buffers(b, S, hq, d)
+        for x in bufs:
+            x.fill_(float("nan"))
+        desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+        cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, *bufs, EMIT | FIN)
+        torch.cuda.synchronize()
+        assert 0.5 < time.time() - t0 < 30.0
+        assert all(torch.isnan(x).all() for x in bufs), "a split launch ran while the status word held an error"
+        assert cpa.cp_take_device_status() == cpa.CP_ERR_TIMEOUT
+        o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        ref_out, _, _, _ = OA.full_causal_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+        assert_out_close(o.cpu().numpy(), ref_out, "split after recovery")
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)  # this module's setting
