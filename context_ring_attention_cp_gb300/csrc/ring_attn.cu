@@ -435,6 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   auto bar_l = [&](int tt) { return smem_u32(&bars[9 + 2 * K::kStages + tt]); };  // old O tile loaded
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(&bars[11 + 2 * K::kStages]);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  // A split launch has one query tile per CTA and three S buffers (TMEM columns 0, 128 and
+  // 384; O at 256): buffer b's S-ready and P-ready barriers are bar_s3(b) and bar_p3(b)
+  // (tile B's slots for buffer 1 and two more for buffer 2), and bar_o(0) completes one
+  // phase per PV.
+  auto bar_s3 = [&](int b) { return b < 2 ? bar_s(b) : smem_u32(&bars[12 + 2 * K::kStages]); };
+  auto bar_p3 = [&](int b) { return b < 2 ? bar_p(b) : smem_u32(&bars[13 + 2 * K::kStages]); };
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -453,6 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       mbar_init(bar_o(tt), 1);
       mbar_init(bar_e(tt), BM / 32);
       mbar_init(bar_l(tt), 1);
+    }
+    if constexpr (SPLIT) {
+      mbar_init(bar_s3(2), 1);
+      mbar_init(bar_p3(2), BM / 32);
     }
     // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) ? 1 : 0;
@@ -586,6 +596,47 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
                     smem_desc(va + kk * 2048, K::kSlab, 1024), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
+      if constexpr (SPLIT) {
+        // One query tile, three S buffers: S of K/V tile j goes to buffer j % 3 and is
+        // issued right after the PV of tile j - 3 (the last reader of that buffer's P),
+        // so the softmax of tile j + 1 need not wait for PV(j).  tcgen05.mma executes in
+        // issue order, so a buffer's P is consumed before the next S overwrites it.
+        auto s3_col = [](int b) { return b == 2 ? 384u : uint32_t(b) * 128u; };
+        auto s_step = [&](int32_t jj) -> bool {
+          const int lk = 2 * jj, sk = lk % K::kStages;
+          if (!wait(bar_full(sk), uint32_t((lk / K::kStages) & 1))) return false;
+          tc_fence_after();
+          const int b = jj % 3;
+          const uint32_t qa = sbase + K::kQOff;
+          const uint32_t ka = sbase + K::kKvOff + sk * K::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * K::kSlab + (kk % 4) * 32;
+            mma_ss_if(is, tmem + s3_col(b), smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024), idesc_s,
+                      kk > 0 ? 1u : 0u);
+          }
+          mma_commit_if(is, bar_s3(b));
+          mma_commit_if(is, bar_empty(sk));  // K_jj consumed
+          return true;
+        };
+        for (int32_t jj = 0; ok && jj < 3 && jj < n_kv; ++jj) ok = s_step(jj);
+        for (int32_t j = 0; ok && j < n_kv; ++j) {
+          const int lv = 2 * j + 1, sv = lv % K::kStages;
+          if (!wait(bar_full(sv), uint32_t((lv / K::kStages) & 1))) { ok = false; break; }
+          const int b = j % 3;
+          if (!wait(bar_p3(b), uint32_t((j / 3) & 1))) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t va = sbase + K::kKvOff + sv * K::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            mma_ts_if(is, tmem + K::kOCol, tmem + s3_col(b) + uint32_t(kk * 8),
+                      smem_desc(va + kk * 2048, K::kSlab, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_if(is, bar_empty(sv));  // V_j consumed
+          mma_commit_if(is, bar_o(0));       // PV(j) done: one phase per K/V tile
+          if (j + 3 < n_kv && !s_step(j + 3)) { ok = false; break; }
+        }
+      } else {
       // prologue: S(0) for both tiles
       if (ok) ok = wait(bar_full(0), 0);
       if (ok) {
@@ -621,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           }
         }
       }
+      }  // !SPLIT
       if (!ok) {
         const uint64_t t0 = globaltimer();
         while (globaltimer() - t0 < 50000ull) {
@@ -662,11 +714,19 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       bool diag = false;
       cur.next(key0, key_end, diag);
       // Warp-uniform outcome: the TMEM accesses below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s(tt), uint32_t(j & 1), abort_flag))) { ok = false; break; }
+      // Split: this tile's S buffer for K/V tile j is j % 3 (its j / 3-th use).
+      const int b3 = SPLIT ? int(j % 3) : tt;
+      const uint32_t s_cur = SPLIT ? tmem + lane_base + (b3 == 2 ? 384u : uint32_t(b3) * 128u) : s_addr;
+      if (!__all_sync(0xffffffffu, mbar_wait(SPLIT ? bar_s3(b3) : bar_s(tt), SPLIT ? uint32_t((j / 3) & 1)
+                                                                                  : uint32_t(j & 1),
+                                             abort_flag))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // Raw logits of this row (the scale is applied inside the exponent's FFMA).
       uint32_t sr[BN];
-      tmem_ld128(s_addr, sr);
+      tmem_ld128(s_cur, sr);
       tmem_ld_wait128(sr);
       float x[BN];
 #pragma unroll
@@ -719,11 +779,17 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           add2(ps8[acc], ps8[acc + 1], ps8[acc], ps8[acc + 1], a, b);
           pk[i] = pack_bf16(a, b);
         }
-        tmem_st64(s_addr, pk);
+        tmem_st64(s_cur, pk);
       }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       // O is rescaled after P is out (the logits are dead by then); PV_T(j)
-      // cannot start before this thread's arrive below.
+      // cannot start before this thread's arrive below.  Split, this S was issued before
+      // PV(j - 1), so first wait for PV(j - 1) (every K/V tile, one phase each).
+      if (SPLIT && j > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar_o(0), uint32_t((j - 1) & 1), abort_flag))) {
+        ok = false;
+        break;
+      }
       if (__any_sync(0xffffffffu, rescale_o)) {
         const float f = rescale_o ? corr : 1.f;
 #pragma unroll
@@ -740,12 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p(tt));  // one arrival per warp (count 4)
+      if (lane == 0) mbar_arrive(SPLIT ? bar_p3(b3) : bar_p(tt));  // one arrival per warp (count 4)
     }
 
     // ---------------- epilogue: this row's triple, merged / normalised as asked
     const bool have = ok && n_kv > 0;
-    if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), 0, abort_flag))) ok = false;
+    if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), SPLIT ? uint32_t((n_kv - 1) & 1) : 0u, abort_flag)))
+      ok = false;
     if (ok) {
       tc_fence_after();
       // Re-express (l, O) against the true max: factor 2^(m_ref - m_true) <= 1.
