@@ -447,6 +447,37 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   const int32_t part = SPLIT ? int32_t(blockIdx.x) % p.kv_split : 0;  // this CTA's rank in its cluster
   const Item it = decode_item<LAYOUT>(p, SPLIT ? int32_t(blockIdx.x) / p.kv_split : int32_t(blockIdx.x));
 
+  if constexpr (!SPLIT) {
+    // An item that sees no key over the step range (a head chunk whose source chunks all
+    // lie after it): merging the identity into a running triple changes nothing, so
+    // ACCUMULATE without FINALIZE leaves it as it is; EMIT writes the identity (O = 0,
+    // m = -inf, l = 0; FINALIZE gives O = 0 as well) with plain stores.  No barrier,
+    // TMEM or copy is set up.  (ACCUMULATE | FINALIZE normalises the old triple below.)
+    if (KvCursor<LAYOUT>::count(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last) == 0) {
+      const bool acc = (p.mode & CP_MODE_ACCUMULATE) != 0;
+      if (acc && (p.mode & CP_MODE_FINALIZE) == 0) return;
+      if (!acc) {
+        if (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) return;  // an earlier wait gave up
+        for (int tt = 0; tt <= it.has_b; ++tt) {
+          const int h = it.h0 + tt * it.dh;
+          const int32_t row0 = it.q_row0 + tt * it.drow;
+          const int32_t rows = tt ? it.q_rows_b : it.q_rows;
+          for (int e = threadIdx.x; e < rows * (D / 4); e += kThreads) {
+            const int32_t row = row0 + e / (D / 4);
+            reinterpret_cast<float4*>(p.o + ((int64_t(it.bi) * p.S + row) * p.h_q + h) * D)[e % (D / 4)] =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int r = threadIdx.x; r < rows; r += kThreads) {
+            const int64_t ml = (int64_t(it.bi) * p.h_q + h) * p.S + row0 + r;
+            p.m[ml] = -INFINITY;
+            p.l[ml] = 0.f;
+          }
+        }
+        return;
+      }
+    }
+  }
+
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < K::kStages; ++s) {
