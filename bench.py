@@ -543,22 +543,30 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
         "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     # the whole ring as cp launches of one step each (the first EMIT, then ACCUMULATE, the
-    # last normalising), as the steps run when each rank launches per step
-    def chain():
+    # last normalising), as the steps run when each rank launches per step; each launch a
+    # programmatic dependent of the one before (its CTAs start in the previous launch's
+    # tail), and for comparison the same launches fully serialised
+    def chain(extra):
         for t in range(w["cp"]):
             md = cpa.CP_MODE_EMIT if t == 0 else cpa.CP_MODE_ACCUMULATE
             if t == w["cp"] - 1:
                 md |= cpa.CP_MODE_FINALIZE
-            cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, o, m, l, md, stream)
+            cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, o, m, l, md | extra, stream)
+    ovl = cpa.CP_MODE_OVERLAP_PREVIOUS
     for _ in range(3):
-        chain()
-    ms = _events_time(chain, 10, stream)
+        chain(ovl)
+        chain(0)
+    ms_serial = _events_time(lambda: chain(0), 10, stream)
+    ms = _events_time(lambda: chain(ovl), 10, stream)
     tf = prefill_flops(w) / (ms * 1e-3) / 1e12
     out["prefill_per_step_chain"] = {
         "workload": "the GQA prefill ring as 8 single-step launches (EMIT, ACCUMULATE..., the last "
-                    "FINALIZE) instead of one fused launch",
+                    "FINALIZE) instead of one fused launch, each overlapping the previous one's tail "
+                    "(CP_MODE_OVERLAP_PREVIOUS)",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": prefill_flops(w),
-        "launches": w["cp"], "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+        "launches": w["cp"], "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
+        "serialised": {"ms": round(ms_serial, 4),
+                       "value": round(prefill_flops(w) / (ms_serial * 1e-3) / 1e12, 1)}}
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # per-virtual-rank work under the balanced (method) and sequential (plain) layouts:

@@ -19,7 +19,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = [
-    "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE",
+    "CpError", "AttnDesc", "CP_MODE_EMIT", "CP_MODE_ACCUMULATE", "CP_MODE_FINALIZE", "CP_MODE_OVERLAP_PREVIOUS",
     "CP_MAX_MERGE_PARTS", "library_path", "load_library", "cp_status_string",
     "cp_ring_attn_host", "cp_ring_attn_host_workspace_bytes",
     "cp_plan_balanced_chunks", "cp_plan_chunks", "cp_comm_bytes", "cp_ring_step_partial_attn",
@@ -38,6 +38,7 @@ CP_ERR_TIMEOUT = 5
 CP_MODE_EMIT = 0
 CP_MODE_ACCUMULATE = 1
 CP_MODE_FINALIZE = 2
+CP_MODE_OVERLAP_PREVIOUS = 4
 CP_LAYOUT_BALANCED = 0
 CP_LAYOUT_SEQUENTIAL = 1
 CP_MAX_MERGE_PARTS = 256

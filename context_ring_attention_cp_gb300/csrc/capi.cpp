@@ -278,7 +278,8 @@ cp_status cp_ring_rank_partial_attn(const cp_attn_desc* desc, int32_t layout, in
   if (layout != CP_LAYOUT_BALANCED && layout != CP_LAYOUT_SEQUENTIAL) return CP_ERR_INVALID_ARGUMENT;
   if (rank_begin < 0 || rank_end <= rank_begin || rank_end > desc->cp) return CP_ERR_INVALID_ARGUMENT;
   if (step_begin < 0 || step_end <= step_begin || step_end > desc->cp) return CP_ERR_INVALID_ARGUMENT;
-  if ((mode & ~(CP_MODE_ACCUMULATE | CP_MODE_FINALIZE)) != 0) return CP_ERR_INVALID_ARGUMENT;
+  if ((mode & ~(CP_MODE_ACCUMULATE | CP_MODE_FINALIZE | CP_MODE_OVERLAP_PREVIOUS)) != 0)
+    return CP_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(m) || !aligned16(l))
     return CP_ERR_INVALID_ARGUMENT;
   if (desc->causal != 1) return CP_ERR_UNSUPPORTED;

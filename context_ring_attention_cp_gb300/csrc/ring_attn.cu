@@ -446,6 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   const int lane = threadIdx.x % 32;
   const int32_t part = SPLIT ? int32_t(blockIdx.x) % p.kv_split : 0;  // this CTA's rank in its cluster
   const Item it = decode_item<LAYOUT>(p, SPLIT ? int32_t(blockIdx.x) / p.kv_split : int32_t(blockIdx.x));
+  // A ring launch that follows this one on the stream with CP_MODE_OVERLAP_PREVIOUS may
+  // start its CTAs as soon as all of this grid's CTAs are running: it touches (o, m, l)
+  // only after grid_dependency_wait, that is, after this grid has finished.
+  grid_launch_dependents();
 
   if constexpr (!SPLIT) {
     // An item that sees no key over the step range (a head chunk whose source chunks all
@@ -457,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       const bool acc = (p.mode & CP_MODE_ACCUMULATE) != 0;
       if (acc && (p.mode & CP_MODE_FINALIZE) == 0) return;
       if (!acc) {
+        grid_dependency_wait();  // the kernel before this one may still own (o, m, l)
         if (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) return;  // an earlier wait gave up
         for (int tt = 0; tt <= it.has_b; ++tt) {
           const int h = it.h0 + tt * it.dh;
@@ -841,6 +846,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     }
 
     // ---------------- epilogue: this row's triple, merged / normalised as asked
+    // (o, m, l) are read and written only from here on: under CP_MODE_OVERLAP_PREVIOUS
+    // the kernel before this one on the stream may have been running until now.
+    grid_dependency_wait();
     const bool have = ok && n_kv > 0;
     if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), SPLIT ? uint32_t((n_kv - 1) & 1) : 0u, abort_flag)))
       ok = false;
@@ -1003,6 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   }
   if constexpr (SPLIT) {
     // warps 4-11 (all 256 of them, whether or not they had a tile) merge the rows
+    grid_dependency_wait();
     cluster_sync_all();
     if (p.kv_split == 2)
       split_merge<D, 2>(p, it, part, smem, sbase);
@@ -1098,6 +1107,22 @@ cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
   if (cudaFuncSetAttribute(ring_attn_kernel<D, LAYOUT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            K::kSmemBytes) != cudaSuccess)
     return CP_ERR_CUDA;
+  if ((p.mode & CP_MODE_OVERLAP_PREVIOUS) != 0) {
+    // Programmatic dependent launch: the CTAs may start while the kernel before this one
+    // on the stream still runs; each waits for it before touching (o, m, l).
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(unsigned(n_items), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = K::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ring_attn_kernel<D, LAYOUT, false>, p) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
+  }
   ring_attn_kernel<D, LAYOUT, false><<<unsigned(n_items), kThreads, K::kSmemBytes, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? CP_OK : CP_ERR_CUDA;
 }

@@ -402,7 +402,15 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
 // Generic-proxy shared-memory writes made visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Named barrier among `count` threads (count a multiple of 32).
+// Programmatic dependent launch.  launch_dependents lets the next kernel on the stream,
+// if it was launched with programmatic stream serialisation, start once every CTA of
+// this grid has issued it (or exited).  grid_dependency_wait blocks the calling thread
+// until the grids this one depends on have completed and their memory is visible; in a
+// kernel launched without that attribute it returns at once.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace tc
 }  // namespace cpattn

@@ -54,11 +54,19 @@ typedef enum {
   CP_ERR_TIMEOUT = 5           /* a device-side wait gave up (reported by cp_take_device_status) */
 } cp_status;
 
-/* Modes of cp_ring_step_partial_attn.  FINALIZE may be OR-ed into either. */
+/* Modes of cp_ring_step_partial_attn.  FINALIZE and OVERLAP_PREVIOUS may be OR-ed
+ * into either of EMIT and ACCUMULATE. */
 enum {
   CP_MODE_EMIT = 0,       /* write the triple of the steps [step_begin, step_end) */
   CP_MODE_ACCUMULATE = 1, /* merge that triple into the triple already in (o, m, l) */
-  CP_MODE_FINALIZE = 2    /* after that, write o = O / l (0 where l = 0); m, l stay */
+  CP_MODE_FINALIZE = 2,   /* after that, write o = O / l (0 where l = 0); m, l stay */
+  /* Launch as a programmatic dependent of the kernel before it on the stream: the
+   * CTAs may start while that kernel still runs, read q, k, v at once and wait for
+   * it to finish before they read or write o, m, l.  The caller promises that the
+   * kernel before this launch on the stream writes none of q, k, v (true in a chain
+   * of ring-step launches over the same inputs, where each launch's tail then
+   * overlaps the next one's start).  The results are the same bits as without it. */
+  CP_MODE_OVERLAP_PREVIOUS = 4
 };
 
 /* Chunk layouts.  BALANCED is the method (Terms table, "Balanced chunk split"):

@@ -205,7 +205,7 @@ def test_ring_rejects_descriptors(cpa, kw, status):
     assert e.value.status == status
 
 
-@pytest.mark.parametrize("t0,t1,mode", [(-1, 1, 0), (1, 1, 0), (0, 3, 0), (2, 1, 0), (0, 2, 4), (0, 2, -1)])
+@pytest.mark.parametrize("t0,t1,mode", [(-1, 1, 0), (1, 1, 0), (0, 3, 0), (2, 1, 0), (0, 2, 8), (0, 2, -1)])
 def test_ring_rejects_steps_and_modes(cpa, t0, t1, mode):
     with pytest.raises(cpa.CpError) as e:
         cpa.cp_ring_step_partial_attn(_desc(cpa), t0, t1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, mode, stream=0)

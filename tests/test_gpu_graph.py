@@ -39,9 +39,12 @@ def _replay(g, stream, times=2):
     torch.cuda.synchronize()
 
 
-def test_ring_step_chain_replays_bit_equal():
+@pytest.mark.parametrize("overlap", [False, True], ids=["plain", "overlapped"])
+def test_ring_step_chain_replays_bit_equal(overlap):
     # cp single-step launches: EMIT, then ACCUMULATE, the last one FINALIZE.  The chain
     # rewrites its whole running triple, so replaying it twice gives the same bits.
+    # Overlapped, the captured launches after the first are programmatic dependents of
+    # the one before (graph edges of that kind); the eager chain they are held to is plain.
     b, S, hq, hkv, d, cp = 1, 4096, 8, 2, 128, 4
     q, k, v = synth.prefill_inputs(b, S, hq, hkv, d, std=0.5, seed=91)
     desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
@@ -51,12 +54,12 @@ def test_ring_step_chain_replays_bit_equal():
         m = torch.full((b, hq, S), float("nan"), dtype=torch.float32, device="cuda")
         return o, m, torch.full_like(m, float("nan"))
 
-    def chain(o, m, l, stream):
+    def chain(o, m, l, stream, extra=0):
         for t in range(cp):
             mode = cpa.CP_MODE_EMIT if t == 0 else cpa.CP_MODE_ACCUMULATE
             if t == cp - 1:
                 mode |= cpa.CP_MODE_FINALIZE
-            cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, o, m, l, mode, stream)
+            cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, o, m, l, mode | extra, stream)
 
     eager = buffers()
     chain(*eager, torch.cuda.current_stream())
@@ -65,7 +68,8 @@ def test_ring_step_chain_replays_bit_equal():
 
     side = torch.cuda.Stream()
     graphed = buffers()
-    g = _capture(lambda st: chain(*graphed, st), side)
+    extra = cpa.CP_MODE_OVERLAP_PREVIOUS if overlap else 0
+    g = _capture(lambda st: chain(*graphed, st, extra), side)
     _replay(g, side)
     assert cpa.cp_take_device_status() == 0
     for x, y in zip(eager, graphed):

@@ -427,6 +427,86 @@ def test_per_step_accumulate_chain_at_full_size():
     torch.cuda.empty_cache()
 
 
+OVL = cpa.CP_MODE_OVERLAP_PREVIOUS
+
+
+def _launch_chain(desc, q, k, v, bufs, cp, extra):
+    # cp single-step launches with no synchronisation between them: EMIT, ACCUMULATE...,
+    # the last one FINALIZE
+    for t in range(cp):
+        md = (EMIT if t == 0 else ACC) | (FIN if t == cp - 1 else 0) | extra
+        cpa.cp_ring_step_partial_attn(desc, t, t + 1, q, k, v, *bufs, md)
+
+
+def _nan_buffers(b, S, hq, d):
+    o, m, l = ring_buffers(b, S, hq, d)
+    for x in (o, m, l):
+        x.fill_(float("nan"))
+    return o, m, l
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"S{c[1]}_h{c[2]}x{c[3]}_d{c[4]}_cp{c[5]}_b{c[0]}" for c in SMALL])
+def test_overlapped_step_chain_gives_the_same_bits(case):
+    # With CP_MODE_OVERLAP_PREVIOUS each launch may start while the one before it runs and
+    # waits for it before touching (o, m, l).  The chain is launched twice in a row into
+    # the same buffers (the second chain's EMIT rewrites rows the first chain's last launch
+    # is finalising) and must give the bits of the same chain with every launch serialised.
+    b, S, hq, hkv, d, cp, std = case
+    q, k, v = _inputs(b, S, hq, hkv, d, std, seed=S + 7 * hq + d)
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+    plain = _nan_buffers(b, S, hq, d)
+    _launch_chain(desc, q, k, v, plain, cp, 0)
+    torch.cuda.synchronize()
+    ovl = _nan_buffers(b, S, hq, d)
+    _launch_chain(desc, q, k, v, ovl, cp, OVL)
+    _launch_chain(desc, q, k, v, ovl, cp, OVL)
+    torch.cuda.synchronize()
+    assert cpa.cp_take_device_status() == 0
+    for x, y in zip(plain, ovl):
+        assert torch.equal(x, y)
+
+
+def test_overlap_flag_on_a_split_launch_changes_nothing():
+    # Launches whose key walks are split over clusters run without the dependent-launch
+    # attribute; the flag must still be accepted and give the same bits.
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, -1)
+    try:
+        b, S, hq, hkv, d, cp = 1, 1024, 4, 4, 64, 2
+        q, k, v = _inputs(b, S, hq, hkv, d, 1.0, seed=4242)
+        desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+        ref = _nan_buffers(b, S, hq, d)
+        cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, *ref, EMIT | FIN)
+        got = _nan_buffers(b, S, hq, d)
+        cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, *got, EMIT | FIN | OVL)
+        cpa.cp_ring_step_partial_attn(desc, 0, cp, q, k, v, *got, EMIT | FIN | OVL)
+        torch.cuda.synchronize()
+        assert cpa.cp_take_device_status() == 0
+        for x, y in zip(ref, got):
+            assert torch.equal(x, y)
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)
+
+
+def test_overlapped_step_chain_at_full_size():
+    # The GQA workload's ring as cp overlapped single-step launches: the same bits as the
+    # serialised chain, whose agreement with the fused ring and the oracle is checked above.
+    w = synth.WORKLOADS["gqa"]
+    b, S, hq, hkv, d, cp = w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"]
+    q, k, v = synth.prefill_inputs(b, S, hq, hkv, d, std=w["std"], seed=w["seed"])
+    desc = cpa.make_desc(b, S, hq, hkv, d, cp, 1.0 / math.sqrt(d), 1)
+    plain = _nan_buffers(b, S, hq, d)
+    _launch_chain(desc, q, k, v, plain, cp, 0)
+    torch.cuda.synchronize()
+    ovl = _nan_buffers(b, S, hq, d)
+    _launch_chain(desc, q, k, v, ovl, cp, OVL)
+    torch.cuda.synchronize()
+    assert cpa.cp_take_device_status() == 0
+    for x, y in zip(plain, ovl):
+        assert torch.equal(x, y)
+    del q, k, v, plain, ovl
+    torch.cuda.empty_cache()
+
+
 # Odd groups (one query head per K/V head, or three): a CTA takes two consecutive 128-row
 # tiles of one head, and the first tile sees one fully masked K/V tile on its chunk's
 # diagonal.  Chunks of 250 rows (a 122-row second tile), 384 rows (a pair and a single
