@@ -172,14 +172,14 @@ def _arg(x, name: str, where: str, dtype=None, numel: int = 0, nbytes: int = 0, 
 
 def _ring_args(desc, q, k, v, o, m, l, where: str, cuda: bool = True, dev: Optional[list] = None):
     import torch
-    b, S, hq, hkv, d = int(desc.b), int(desc.S), int(desc.h_q), int(desc.h_kv), int(desc.d)
+    b, S, hq, hkv, d = desc.b, desc.S, desc.h_q, desc.h_kv, desc.d  # ctypes fields read as ints
+    n_q, n_kv, n_ml = b * S * hq * d, b * S * hkv * d, b * hq * S
     dev = [None] if dev is None else dev
-    return (_arg(q, "q", where, torch.bfloat16, b * S * hq * d, cuda=cuda, dev=dev),
-            _arg(k, "k", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
-            _arg(v, "v", where, torch.bfloat16, b * S * hkv * d, cuda=cuda, dev=dev),
-            _arg(o, "o", where, torch.float32, b * S * hq * d, cuda=cuda, dev=dev),
-            _arg(m, "m", where, torch.float32, b * hq * S, cuda=cuda, dev=dev),
-            _arg(l, "l", where, torch.float32, b * hq * S, cuda=cuda, dev=dev))
+    bf16, f32 = torch.bfloat16, torch.float32
+    # positional arguments: this runs on every launch, and a latency-bound caller feels it
+    return (_arg(q, "q", where, bf16, n_q, 0, cuda, dev), _arg(k, "k", where, bf16, n_kv, 0, cuda, dev),
+            _arg(v, "v", where, bf16, n_kv, 0, cuda, dev), _arg(o, "o", where, f32, n_q, 0, cuda, dev),
+            _arg(m, "m", where, f32, n_ml, 0, cuda, dev), _arg(l, "l", where, f32, n_ml, 0, cuda, dev))
 
 
 def _merge_args(batch, rows, heads, d, n_parts, o_parts, m_parts, l_parts, o_out, m_out, l_out, where: str):

@@ -25,6 +25,44 @@ cudaError_t cpattn::current_sm_count(int* sms) {
   return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
 }
 
+// Id of the calling thread's current context, 0 when it cannot be read.  A device
+// reset destroys the current context; the next one has a new id.
+unsigned long long cpattn::current_context_id() {
+  struct Fns {
+    PFN_cuCtxGetCurrent_v4000 get_current;
+    PFN_cuCtxGetId_v12000 get_id;
+  };
+  static const Fns fns = []() {
+    Fns f{nullptr, nullptr};
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.get_current == nullptr || fns.get_id == nullptr || fns.get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || fns.get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+cudaError_t cpattn::raise_smem_limit(const void* func, int bytes, SmemLimit* lim) {
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(lim->mu);
+  if (ctx != 0 && lim->ctx == ctx && lim->bytes >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  lim->ctx = ctx;  // the context's limit is now exactly `bytes`
+  lim->bytes = bytes;
+  return cudaSuccess;
+}
+
 namespace {
 constexpr int kKnobs = 3;
 std::atomic<int32_t> g_kernel_choice[kKnobs] = {{-1}, {-1}, {-1}};

@@ -345,33 +345,6 @@ struct ScratchAddr {
 };
 ScratchAddr g_noalloc_addr[kMaxDevices] = {};
 
-// Id of the calling thread's current context, 0 when it cannot be read.  A device
-// reset destroys the context that holds the array; the next context has a new id.
-unsigned long long current_context_id() {
-  struct Fns {
-    PFN_cuCtxGetCurrent_v4000 get_current;
-    PFN_cuCtxGetId_v12000 get_id;
-  };
-  static const Fns fns = []() {
-    Fns f{nullptr, nullptr};
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-    return f;
-  }();
-  CUcontext ctx = nullptr;
-  unsigned long long id = 0;
-  if (fns.get_current == nullptr || fns.get_id == nullptr || fns.get_current(&ctx) != CUDA_SUCCESS ||
-      ctx == nullptr || fns.get_id(ctx, &id) != CUDA_SUCCESS)
-    return 0;
-  return id;
-}
-
 }  // namespace
 
 size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchFloats * sizeof(float); }

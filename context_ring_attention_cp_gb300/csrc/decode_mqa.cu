@@ -512,8 +512,8 @@ bool encode(CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_
 template <int D, int G>
 cudaError_t launch_dg(const MqaParams& p, dim3 grid, cudaStream_t stream) {
   using K = MqaCfg<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(mqa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       K::kSmemBytes);
+  static SmemLimit lim;
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(mqa_decode_kernel<D, G>), K::kSmemBytes, &lim);
   if (e != cudaSuccess) return e;
   mqa_decode_kernel<D, G><<<grid, kThreads, K::kSmemBytes, stream>>>(p);
   return cudaGetLastError();

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/cpattn.h"
 
 namespace cpattn {
@@ -18,6 +20,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t current_sm_count(int* sms);
 // Current value of a cp_set_kernel_choice knob (-1 = automatic).
 int32_t kernel_choice(int32_t knob);
+// Id of the calling thread's current CUDA context (0 when none can be read).
+unsigned long long current_context_id();
+// A kernel's dynamic shared-memory limit, raised with cudaFuncSetAttribute only when the
+// current context has not yet been given at least `bytes` (the attribute belongs to the
+// context's copy of the kernel: another device, or a device reset, needs it again).
+// One SmemLimit per kernel (function-local static); calls may come from any thread.
+struct SmemLimit {
+  std::mutex mu;
+  unsigned long long ctx = 0;
+  int bytes = 0;
+};
+cudaError_t raise_smem_limit(const void* func, int bytes, SmemLimit* lim);
 
 // ---- LSE merge (merge.cu) --------------------------------------------------
 struct MergeParams {

@@ -643,10 +643,12 @@ cudaError_t launch_merge_tree(const MergeParams& p, cudaStream_t stream) {
   switch (lg) {
 #define CPATTN_TREE_CASE(L)                                                                                      \
   case L:                                                                                                        \
-    if (smem > 48 * 1024 && cudaFuncSetAttribute(lse_merge_tree_kernel<L>,                                       \
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=      \
-                                cudaSuccess)                                                                     \
-      return cudaErrorInvalidValue;                                                                              \
+    if (smem > 48 * 1024) {                                                                                      \
+      static SmemLimit lim;                                                                                      \
+      if (raise_smem_limit(reinterpret_cast<const void*>(lse_merge_tree_kernel<L>), int(smem), &lim) !=          \
+          cudaSuccess)                                                                                           \
+        return cudaErrorInvalidValue;                                                                            \
+    }                                                                                                            \
     lse_merge_tree_kernel<L><<<unsigned(ctas), kTreeThreads, smem, stream>>>(p, rows_per_cta);                   \
     break;
     CPATTN_TREE_CASE(1) CPATTN_TREE_CASE(2) CPATTN_TREE_CASE(3) CPATTN_TREE_CASE(4)
@@ -687,7 +689,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const size_t tsmem = merge_tma_smem_bytes(p.n_parts);
-    cudaError_t e = cudaFuncSetAttribute(lse_merge_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(tsmem));
+    static SmemLimit lim_tma;
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(lse_merge_tma_kernel), int(tsmem), &lim_tma);
     if (e != cudaSuccess) return e;
     lse_merge_tma_kernel<<<unsigned(tiles), kThreads, tsmem, stream>>>(tp);
     return cudaGetLastError();
@@ -697,10 +700,11 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   switch (nch) {
 #define CP_MERGE_CASE(N)                                                                       \
-  case N:                                                                                      \
-    e = cudaFuncSetAttribute(lse_merge_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             int(smem));                                                       \
+  case N: {                                                                                    \
+    static SmemLimit lim;                                                                      \
+    e = raise_smem_limit(reinterpret_cast<const void*>(lse_merge_kernel<N>), int(smem), &lim); \
     if (e != cudaSuccess) return e;                                                            \
+  }                                                                                            \
     lse_merge_kernel<N><<<unsigned(tiles), kThreads, smem, stream>>>(p);                       \
     break;
     CP_MERGE_CASE(1)

@@ -1087,7 +1087,8 @@ cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
   if (LAYOUT == CP_LAYOUT_BALANCED && p.kv_split > 1) {
     // One cluster of kv_split CTAs per item (at most 8, the portable cluster size).
     auto kern = ring_attn_kernel<D, CP_LAYOUT_BALANCED, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSplitSmemBytes) != cudaSuccess)
+    static SmemLimit lim_split;
+    if (raise_smem_limit(reinterpret_cast<const void*>(kern), K::kSplitSmemBytes, &lim_split) != cudaSuccess)
       return CP_ERR_CUDA;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -1104,8 +1105,9 @@ cp_status launch_d(const RingParams& p, int64_t n_items, cudaStream_t stream) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? CP_OK : CP_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(ring_attn_kernel<D, LAYOUT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           K::kSmemBytes) != cudaSuccess)
+  static SmemLimit lim;
+  if (raise_smem_limit(reinterpret_cast<const void*>(ring_attn_kernel<D, LAYOUT, false>), K::kSmemBytes, &lim) !=
+      cudaSuccess)
     return CP_ERR_CUDA;
   if ((p.mode & CP_MODE_OVERLAP_PREVIOUS) != 0) {
     // Programmatic dependent launch: the CTAs may start while the kernel before this one
