@@ -46,6 +46,9 @@ import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 WORKLOAD = "gqa"
+# Seeded random rows per head in the long workload's cpu_baseline sample (one head per kv
+# head): about 10 s of fp64 work on 16 cores.
+LONG_BASELINE_ROWS = 1536
 METRIC = "ring-step prefill TFLOP/s (% bf16 peak); pass-Q decode GB/s (% HBM peak)"
 
 
@@ -490,7 +493,7 @@ def bench_ours(args, rank, world, dist):
     cpu = None
     if pool is not None:
         # every head x the sampled rows of this workload (the inputs timed above)
-        cpu = oracle_prefill_leg(pool, w, q, k, v, list(range(hq)), args.cpu_random_rows, seed=w["seed"])
+        cpu = oracle_prefill_leg(pool, w, q, k, v, list(range(hq)), args.cpu_baseline_rows, seed=w["seed"])
         pool.close()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
@@ -610,7 +613,8 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                            "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     if pool is not None:  # one query head per kv head x the sampled rows
         g = w["h_q"] // w["h_kv"]
-        out["prefill_long"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(0, w["h_q"], g)), 64,
+        out["prefill_long"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(0, w["h_q"], g)),
+                                                                 LONG_BASELINE_ROWS,
                                                                  seed=w["seed"])
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
@@ -897,7 +901,10 @@ def main():
     ap.add_argument("--cpu-workers", type=int, default=os.cpu_count() or 1,
                     help="oracle worker processes (default: every host core)")
     ap.add_argument("--cpu-random-rows", type=int, default=64,
-                    help="seeded random rows per head in the oracle's prefill sample")
+                    help="seeded random rows per head in each step's sample of the reference arm")
+    ap.add_argument("--cpu-baseline-rows", type=int, default=2048,
+                    help="seeded random rows per head in the headline's cpu_baseline sample "
+                         "(about 10 s of fp64 work on 16 cores)")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
