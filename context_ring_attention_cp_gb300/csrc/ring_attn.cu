@@ -93,6 +93,10 @@ struct Cfg {
   static constexpr int kSplitOff = kBarOff + 1024;
   static constexpr int kSplitSmemBytes = kSmemBytes + 2048;
   static constexpr uint32_t kOCol = 256;
+  // d = 64 (unsplit): O takes columns 256-383, so P gets columns of its own, 384 + 64 tt,
+  // and S is free as soon as the softmax has read it.
+  static constexpr bool kEarlyS = D == 64;
+  static constexpr uint32_t kPCol = 384;
 };
 
 struct RingParams {
@@ -441,6 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
   // phase per PV.
   auto bar_s3 = [&](int b) { return b < 2 ? bar_s(b) : smem_u32(&bars[12 + 2 * K::kStages]); };
   auto bar_p3 = [&](int b) { return b < 2 ? bar_p(b) : smem_u32(&bars[13 + 2 * K::kStages]); };
+  // Unsplit at d = 64, P lives apart from S: bar_sf(tt) completes when the tile's four
+  // softmax warps have read S (the next S may then be issued into it), and bar_o(tt)
+  // completes once per PV, which the softmax waits for before it reuses the P columns
+  // or rescales O.
+  constexpr bool kEarlyS = K::kEarlyS && !SPLIT;
+  auto bar_sf = [&](int tt) { return smem_u32(&bars[14 + 2 * K::kStages + tt]); };
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -499,6 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     if constexpr (SPLIT) {
       mbar_init(bar_s3(2), 1);
       mbar_init(bar_p3(2), BM / 32);
+    }
+    if constexpr (kEarlyS) {
+      mbar_init(bar_sf(0), BM / 32);
+      mbar_init(bar_sf(1), BM / 32);
     }
     // An earlier wait gave up: the whole CTA skips its work (decided once, CTA-uniform).
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(&g_ring_status) != 0) ? 1 : 0;
@@ -626,9 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       };
       auto issue_pv = [&](int tt, int slot, bool accumulate) {
         const uint32_t va = sbase + K::kKvOff + slot * K::kTileBytes;
+        const uint32_t pa = kEarlyS ? K::kPCol + uint32_t(tt * 64) : s_col[tt];  // P's columns
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts_if(is, tmem + o_col[tt], tmem + s_col[tt] + uint32_t(kk * 8),
+          mma_ts_if(is, tmem + o_col[tt], tmem + pa + uint32_t(kk * 8),
                     smem_desc(va + kk * 2048, K::kSlab, 1024), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
       };
@@ -671,6 +686,45 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           mma_commit_if(is, bar_empty(sv));  // V_j consumed
           mma_commit_if(is, bar_o(0));       // PV(j) done: one phase per K/V tile
           if (j + 3 < n_kv && !s_step(j + 3)) { ok = false; break; }
+        }
+      } else if constexpr (kEarlyS) {
+        // S(j + 1) of a tile is issued as soon as its softmax has read S(j) and K_{j+1} is in,
+        // so it runs during that softmax; PV(j) follows once P(j) is stored.  bar_o(tt)
+        // completes after every PV.  Per K/V tile the order is S_A(j + 1), PV_A(j),
+        // S_B(j + 1), PV_B(j), so tile B's last PV is the last MMA and tile A's comes after
+        // every S: the epilogue's staging (tile A in the Q tiles, tile B in K/V slots)
+        // relies on that.  (Both S before both PV measured 1 % slower on row-paired tiles
+        // and 2-4 % faster on head-paired ones; a warp that polls both tiles and issues
+        // whichever MMA is ready was slower than either and breaks that staging order.)
+        if (ok) ok = wait(bar_full(0), 0);
+        if (ok) {
+          tc_fence_after();
+          for (int tt = 0; tt < n_q; ++tt) {
+            issue_s(tt, 0);
+            mma_commit_if(is, bar_s(tt));
+          }
+          mma_commit_if(is, bar_empty(0));
+        }
+        for (int32_t j = 0; ok && j < n_kv; ++j) {
+          const int lv = 2 * j + 1, lk = 2 * j + 2;
+          const int sv = lv % K::kStages, sk = lk % K::kStages;
+          const bool more = (j + 1 < n_kv);
+          if (more && !wait(bar_full(sk), uint32_t((lk / K::kStages) & 1))) { ok = false; break; }
+          if (!wait(bar_full(sv), uint32_t((lv / K::kStages) & 1))) { ok = false; break; }
+          for (int tt = 0; tt < n_q; ++tt) {
+            if (more) {
+              if (!wait(bar_sf(tt), uint32_t(j & 1))) { ok = false; break; }
+              tc_fence_after();
+              issue_s(tt, sk);
+              mma_commit_if(is, bar_s(tt));
+              if (tt == n_q - 1) mma_commit_if(is, bar_empty(sk));  // K_{j+1} consumed by every tile
+            }
+            if (!wait(bar_p(tt), uint32_t(j & 1))) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(tt, sv, j > 0);
+            mma_commit_if(is, bar_o(tt));
+            if (tt == n_q - 1) mma_commit_if(is, bar_empty(sv));  // V_j consumed by every tile
+          }
         }
       } else {
       // prologue: S(0) for both tiles
@@ -733,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     const uint32_t lane_base = uint32_t((warp % 4) * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + uint32_t(tt * 128);
     const uint32_t o_addr = tmem + lane_base + K::kOCol + uint32_t(tt * D);
+    const uint32_t p_addr = tmem + lane_base + K::kPCol + uint32_t(tt * 64);  // d = 64 unsplit
     float m_ref = -INFINITY;   // exponent reference (log2 units)
     float m_true = -INFINITY;  // true running max (log2 units)
     float l_run = 0.f;
@@ -764,6 +819,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       uint32_t sr[BN];
       tmem_ld128(s_cur, sr);
       tmem_ld_wait128(sr);
+      if constexpr (kEarlyS) {  // S is in registers: the next S may overwrite its columns
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sf(tt));
+      }
       float x[BN];
 #pragma unroll
       for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(sr[i]);
@@ -815,8 +875,19 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           add2(ps8[acc], ps8[acc + 1], ps8[acc], ps8[acc + 1], a, b);
           pk[i] = pack_bf16(a, b);
         }
-        tmem_st64(s_cur, pk);
+        if constexpr (kEarlyS) {
+          // P's columns and O are free once PV(j - 1) has completed (S(j) no longer implies it).
+          if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), uint32_t((j - 1) & 1), abort_flag)))
+            ok = false;
+          if (ok) {
+            tc_fence_after();
+            tmem_st64(p_addr, pk);
+          }
+        } else {
+          tmem_st64(s_cur, pk);
+        }
       }
+      if (!ok) break;
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       // O is rescaled after P is out (the logits are dead by then); PV_T(j)
       // cannot start before this thread's arrive below.  Split, this S was issued before
@@ -850,7 +921,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
     // the kernel before this one on the stream may have been running until now.
     grid_dependency_wait();
     const bool have = ok && n_kv > 0;
-    if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), SPLIT ? uint32_t((n_kv - 1) & 1) : 0u, abort_flag)))
+    if (have && !__all_sync(0xffffffffu, mbar_wait(bar_o(tt), (SPLIT || kEarlyS) ? uint32_t((n_kv - 1) & 1) : 0u,
+                                                   abort_flag)))
       ok = false;
     if (ok) {
       tc_fence_after();
