@@ -258,12 +258,14 @@ class OraclePool:
         return {"cores": self.workers, "host_cpus": os.cpu_count()}
 
 
-def oracle_prefill_leg(pool, w, q, k, v, heads, n_random, seed, full_rows=False):
+def oracle_prefill_leg(pool, w, q, k, v, heads, n_random, seed, full_rows=False, run=True):
     """The oracle on sampled rows (or every row) of a prefill workload; b = 1.
 
     Sample (per head in ``heads``): the first and last row of each of the 2cp chunks, rows 0
     and S-1, and ``n_random`` seeded random rows; ``full_rows`` takes every row instead.
-    Returns the cpu_baseline object: fp64 TFLOP/s, rows/s and the full-config time."""
+    Returns the cpu_baseline object: fp64 TFLOP/s, rows/s and the full-config time.  With
+    ``run=False`` the inputs are written out now and a callable that runs the oracle and
+    returns that object is returned instead."""
     from context_ring_attention_cp_gb300 import synth
     S, d, g = w["S"], w["d"], w["h_q"] // w["h_kv"]
     rows = list(range(S)) if full_rows else synth.sample_rows(S, w["cp"], n_random, seed)
@@ -278,7 +280,13 @@ def oracle_prefill_leg(pool, w, q, k, v, heads, n_random, seed, full_rows=False)
             sel = list(range(part, len(rows), per_head))
             if sel:
                 tasks.append((qpath, kpath, vpath, h, h // g, [rows[i] for i in sel], sel, 1.0 / math.sqrt(d)))
-    flops, nrows, wall = pool.run(_oracle_prefill_rows_task, tasks)
+    job = lambda: _prefill_leg_result(pool, w, heads, rows, n_random, full_rows, tasks,  # noqa: E731
+                                      *pool.run(_oracle_prefill_rows_task, tasks))
+    return job() if run else job
+
+
+def _prefill_leg_result(pool, w, heads, rows, n_random, full_rows, tasks, flops, nrows, wall):
+    S = w["S"]
     rate = flops / wall
     full_flops = prefill_flops(w)
     out = {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "kind": "oracle", **pool.describe(),
@@ -296,9 +304,10 @@ def oracle_prefill_leg(pool, w, q, k, v, heads, n_random, seed, full_rows=False)
     return out
 
 
-def oracle_decode_leg(pool, w, q, k, v, pairs):
+def oracle_decode_leg(pool, w, q, k, v, pairs, run=True):
     """The oracle's pass-Q shard triples for the sampled (sequence, head) pairs, every shard
-    of each pair a task; GB/s of bf16 K/V read, and the full-config time extrapolated."""
+    of each pair a task; GB/s of bf16 K/V read, and the full-config time extrapolated.
+    ``run=False``: as for the prefill leg."""
     from context_ring_attention_cp_gb300 import synth
     L, cp, d, g = w["S"], w["cp"], w["d"], w["h_q"] // w["h_kv"]
     n = L // cp
@@ -309,7 +318,13 @@ def oracle_decode_leg(pool, w, q, k, v, pairs):
             kpath = pool.save(synth.bf16_bits(k[bi, s * n:(s + 1) * n, h // g]))
             vpath = pool.save(synth.bf16_bits(v[bi, s * n:(s + 1) * n, h // g]))
             tasks.append((qpath, kpath, vpath, 1.0 / math.sqrt(d)))
-    nbytes, _, wall = pool.run(_oracle_decode_shard_task, tasks)
+    job = lambda: _decode_leg_result(pool, w, pairs, tasks, *pool.run(_oracle_decode_shard_task, tasks))  # noqa
+    return job() if run else job
+
+
+def _decode_leg_result(pool, w, pairs, tasks, nbytes, _, wall):
+    L, cp, d = w["S"], w["cp"], w["d"]
+    n = L // cp
     rate = nbytes / wall
     full = 2 * w["b"] * L * w["h_q"] * d * 2
     return {"value": round(rate / 1e9, 4), "unit": "GB/s", "kind": "oracle", **pool.describe(),
@@ -320,9 +335,10 @@ def oracle_decode_leg(pool, w, q, k, v, pairs):
                       f"{len(tasks)} tasks on {pool.workers} single-threaded spawn workers"}
 
 
-def oracle_merge_leg(pool, w, po, pm, pl, heads):
+def oracle_merge_leg(pool, w, po, pm, pl, heads, run=True):
     """The oracle's left fold over all parts for every row of the sampled heads, in row
-    blocks; GB/s of fp32 triples read and written, and the full-config time extrapolated."""
+    blocks; GB/s of fp32 triples read and written, and the full-config time extrapolated.
+    ``run=False``: as for the prefill leg."""
     R = w["rows"]
     blocks = max(1, (2 * pool.workers + len(heads) - 1) // len(heads))
     step = (R + blocks - 1) // blocks
@@ -332,7 +348,12 @@ def oracle_merge_leg(pool, w, po, pm, pl, heads):
         lpath = pool.save(pl[:, 0, h, :].cpu().numpy())
         opath = pool.save(po[:, 0, :, h].cpu().numpy())
         tasks += [(mpath, lpath, opath, r0, min(R, r0 + step)) for r0 in range(0, R, step)]
-    nbytes, _, wall = pool.run(_oracle_merge_task, tasks)
+    job = lambda: _merge_leg_result(pool, w, heads, tasks, *pool.run(_oracle_merge_task, tasks))  # noqa: E731
+    return job() if run else job
+
+
+def _merge_leg_result(pool, w, heads, tasks, nbytes, _, wall):
+    R = w["rows"]
     rate = nbytes / wall
     return {"value": round(rate / 1e9, 4), "unit": "GB/s", "kind": "oracle", **pool.describe(),
             "seconds": round(wall, 3),
@@ -513,6 +534,10 @@ def bench_ours(args, rank, world, dist):
 def secondary_lines(cpa, synth, peaks, stream, pool=None):
     import torch
     out = {}
+    # The oracle legs' inputs are written out beside each GPU line, but the legs run after
+    # the last GPU line: right after the long workload's leg (about 8 s on every host core)
+    # the next two GPU lines measured 5-6 % lower than in a run without it.
+    cpu_jobs = []
     # one ring step (t = 1) of all cp virtual ranks on the GQA workload, EMIT: the spec's
     # per-step unit of work, cp * 2C^2 visible pairs per head (F_attn / cp per step in all)
     w = synth.WORKLOADS[WORKLOAD]
@@ -613,9 +638,8 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                            "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
     if pool is not None:  # one query head per kv head x the sampled rows
         g = w["h_q"] // w["h_kv"]
-        out["prefill_long"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(0, w["h_q"], g)),
-                                                                 LONG_BASELINE_ROWS,
-                                                                 seed=w["seed"])
+        cpu_jobs.append(("prefill_long", oracle_prefill_leg(pool, w, q, k, v, list(range(0, w["h_q"], g)),
+                                                            LONG_BASELINE_ROWS, seed=w["seed"], run=False)))
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # multi-head prefill: b1, 32/32 heads, d128, S32768, cp8 (the GQA workload's FLOPs with
@@ -684,8 +708,8 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                            "flops": prefill_flops(w), "peak": peaks["bf16_tflops"],
                            "frac": round(tf / peaks["bf16_tflops"], 4)}
     if pool is not None:  # the whole workload: every row of every head
-        out["prefill_tiny"]["cpu_baseline"] = oracle_prefill_leg(pool, w, q, k, v, list(range(w["h_q"])), 0,
-                                                                 seed=w["seed"], full_rows=True)
+        cpu_jobs.append(("prefill_tiny", oracle_prefill_leg(pool, w, q, k, v, list(range(w["h_q"])), 0,
+                                                            seed=w["seed"], full_rows=True, run=False)))
     del q, k, v, o, m, l
     torch.cuda.empty_cache()
     # pass-Q decode: b8, 16 heads, d512, L131072, cp8 (34.4 GB of K/V)
@@ -705,7 +729,7 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "launches_per_call": 2}
     if pool is not None:  # 16 (sequence, head) pairs, two per sequence, every shard of each
         pairs = [(bi, h) for bi in range(w["b"]) for h in (bi % w["h_q"], (bi + 8) % w["h_q"])]
-        out["decode"]["cpu_baseline"] = oracle_decode_leg(pool, w, q, k, v, pairs)
+        cpu_jobs.append(("decode", oracle_decode_leg(pool, w, q, k, v, pairs, run=False)))
     del q, k, v, ws
     torch.cuda.empty_cache()
     # pass-Q decode with 16 query heads sharing one 512-wide K/V head (MQA / MLA-style), tensor cores
@@ -745,7 +769,7 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                     "unit": "GB/s", "ms": round(ms, 4), "bytes": merge_bytes(w), "peak": peaks["hbm_gbs"],
                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
     if pool is not None:  # every row of 16 of the 64 heads
-        out["merge"]["cpu_baseline"] = oracle_merge_leg(pool, w, po, pm, pl, list(range(0, w["heads"], 4)))
+        cpu_jobs.append(("merge", oracle_merge_leg(pool, w, po, pm, pl, list(range(0, w["heads"], 4)), run=False)))
     # the same 32 parts reduced as the log-depth halving tree (5 levels of pairwise
     # merges), computed in one pass
     nbytes = cpa.cp_merge_tree_workspace_bytes(1, w["rows"], w["heads"], w["d"], w["parts"])
@@ -760,6 +784,8 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
                          "peak": peaks["hbm_gbs"], "frac": round(gbs_tree / peaks["hbm_gbs"], 4), "launches": 1}
     del po, pm, pl, mo
     torch.cuda.empty_cache()
+    for key, job in cpu_jobs:
+        out[key]["cpu_baseline"] = job()
     return out
 
 
