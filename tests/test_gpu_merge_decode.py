@@ -162,6 +162,51 @@ def test_tree_merge_matches_oracle_and_flat_merge(shape):
             assert_rowwise_rel(to[bi].cpu().numpy(), ref, MERGE_REL, f"tree vs oracle {shape}")
 
 
+def _random_merge_cases(n, seed):
+    # Seeded random merges: 1-64 parts in a random fold order (and, for a power-of-two
+    # count, the halving tree), batch 1-2, 1-199 rows, 1-5 heads, d any multiple of 4 up to
+    # 512 (so both the register and the TMA-fed kernels run), ~1 % identity entries.
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        parts = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 13, 16, 31, 32, 47, 64]))
+        d = int(rng.choice([4, 8, 36, 64, 128, 128, 200, 256, 512]))
+        cases.append((parts, int(rng.integers(1, 3)), int(rng.integers(1, 200)), int(rng.integers(1, 6)), d))
+    return cases
+
+
+MERGE_RANDOM = _random_merge_cases(24, 20260103)
+
+
+@pytest.mark.parametrize("shape", MERGE_RANDOM, ids=[f"r{i}" for i in range(len(MERGE_RANDOM))])
+def test_random_merges_against_the_oracle(shape):
+    n, b, rows, heads, d = shape
+    draws = [synth.merge_parts(n, heads, rows, d, spread=80.0, seed=13 * n + d + rows + bi) for bi in range(b)]
+    o = torch.cat([x[0] for x in draws], dim=1).contiguous()
+    m = torch.cat([x[1] for x in draws], dim=1).contiguous()
+    l = torch.cat([x[2] for x in draws], dim=1).contiguous()
+    order = np.random.default_rng(n + rows).permutation(n)
+    tree = n >= 2 and (n & (n - 1)) == 0
+    for fin in (False, True):
+        go, gm, gl = _merge(o, m, l, order=order, finalize=fin)
+        if tree:
+            to, tm, tl = _merge_tree(o, m, l, finalize=fin)
+        torch.cuda.synchronize()
+        for bi in range(b):
+            parts = [(m[p, bi].T.cpu().double().numpy(), l[p, bi].T.cpu().double().numpy(),
+                      o[p, bi].cpu().double().numpy()) for p in range(n)]
+            rm, rl, ro = OR.merge_in_order(parts, order)
+            assert np.array_equal(gm[bi].T.cpu().double().numpy(), rm)
+            assert np.abs(gl[bi].T.cpu().double().numpy() - rl).max() <= MERGE_REL * max(1.0, np.abs(rl).max())
+            ref = OR.finalize((rm, rl, ro))[0] if fin else ro
+            assert_rowwise_rel(go[bi].cpu().numpy(), ref, MERGE_REL, f"merge {shape} fin={fin}")
+            if tree:
+                hm, hl, ho = OR.merge_tree_halves(parts)
+                assert np.array_equal(tm[bi].T.cpu().double().numpy(), hm)
+                href = OR.finalize((hm, hl, ho))[0] if fin else ho
+                assert_rowwise_rel(to[bi].cpu().numpy(), href, MERGE_REL, f"tree {shape} fin={fin}")
+
+
 def test_tree_merge_rejects_bad_part_counts():
     o, m, l = synth.merge_parts(3, 2, 8, 8, seed=1)
     with pytest.raises(cpa.CpError):
@@ -251,6 +296,43 @@ def test_decode_matches_oracle(case):
     lse = (mo + torch.log(lo)).cpu().numpy()
     assert np.abs(lse - (ref_m + np.log(ref_l))).max() <= LSE_ABS
     assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
+
+
+def _random_decode_cases(n, seed):
+    # Seeded random pass-Q decode problems: the SIMT kernel (groups 1, 2, 4; d up to 512
+    # with g * d <= 1024) and the shared-K/V tensor-core kernel (groups 16, 32; d 128-512),
+    # shard lengths 1-1499 (ragged key tiles and single keys), cp 1-8, batch 1-3.
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        cp = int(rng.choice([1, 2, 3, 4, 5, 8]))
+        shard = int(rng.integers(1, 1500))
+        b = int(rng.integers(1, 4))
+        if rng.random() < 0.5:
+            d = int(rng.choice([64, 128, 256, 512]))
+            g = int(rng.choice([g for g in (1, 2, 4) if g * d <= 1024]))
+            hkv = int(rng.integers(1, 5))
+        else:
+            d = int(rng.choice([128, 256, 512]))
+            g = int(rng.choice([16, 32]))
+            hkv = int(rng.integers(1, 3))
+        cases.append((b, cp * shard, hkv * g, hkv, d, cp))
+    return cases
+
+
+DECODE_RANDOM = _random_decode_cases(24, 20260102)
+
+
+@pytest.mark.parametrize("case", DECODE_RANDOM, ids=[f"r{i}" for i in range(len(DECODE_RANDOM))])
+def test_random_decode_problems_against_the_oracle(case):
+    b, L, hq, hkv, d, cp = case
+    q, k, v = synth.decode_inputs(b, L, hq, hkv, d, seed=7 * L + d + hq)
+    out, mo, lo = _decode(q, k, v, cp)
+    ref_out, ref_m, ref_l = OA.decode_attention(f64(q), f64(k), f64(v), 1.0 / math.sqrt(d))
+    assert_out_close(out.cpu().numpy(), ref_out, f"decode {case}")
+    assert np.abs(mo.cpu().numpy() - ref_m).max() <= LSE_ABS
+    lse = (mo + torch.log(lo)).cpu().numpy()
+    assert np.abs(lse - (ref_m + np.log(ref_l))).max() <= LSE_ABS
 
 
 # Query heads sharing one K/V head (MQA / MLA-style): the tensor-core decode kernel.

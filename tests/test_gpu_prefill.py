@@ -373,6 +373,65 @@ def test_grouped_item_order_writes_every_row_once(S):
     torch.cuda.empty_cache()
 
 
+def _random_cases(n, seed):
+    # Seeded random problems within what the oracle finishes in about a second each:
+    # chunk lengths 1-299 (ragged tiles and single tokens), cp 1-8, GQA groups 1-4,
+    # both head dimensions, batch 1-2, the workloads' two input scales (the output
+    # tolerance is absolute, and P's bf16 rounding error grows with |V|), a random step
+    # range and a random kernel choice (tile pairing and key-walk split automatic or forced).
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        cp = int(rng.choice([1, 2, 3, 4, 5, 8]))
+        C = int(rng.integers(1, 300))
+        hkv, g = int(rng.integers(1, 4)), int(rng.choice([1, 2, 3, 4]))
+        b = int(rng.choice([1, 2]))
+        S = 2 * cp * C
+        if S > 1600 or hkv * g > 8 or b * S * hkv * g > 6400:
+            continue
+        d = int(rng.choice([64, 128]))
+        std = float(rng.choice([0.5, 1.0]))
+        t0 = int(rng.integers(0, cp))
+        t1 = int(rng.integers(t0 + 1, cp + 1))
+        pairing, split = int(rng.choice([-1, 0, 1])), int(rng.choice([-1, 0]))
+        cases.append((b, S, hkv * g, hkv, d, cp, std, t0, t1, pairing, split))
+    return cases
+
+
+RANDOM = _random_cases(48, 20260101)
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=[f"r{i}" for i in range(len(RANDOM))])
+def test_random_shapes_and_step_ranges_against_the_oracle(case):
+    b, S, hq, hkv, d, cp, std, t0, t1, pairing, split = case
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, pairing)
+    cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, split)
+    try:
+        q, k, v = _inputs(b, S, hq, hkv, d, std, seed=1000 + S + hq + d)
+        qf, kf, vf = f64(q), f64(k), f64(v)
+        scale = 1.0 / math.sqrt(d)
+        # the whole ring, finalised
+        o, m, l = run_ring(q, k, v, cp, 0, cp, EMIT | FIN)
+        ref_out, ref_m, ref_l, _ = OA.full_causal_attention(qf, kf, vf, scale)
+        assert_out_close(o.cpu().numpy(), ref_out, f"out {case}")
+        assert np.abs((m + torch.log(l)).cpu().numpy() - (ref_m + np.log(ref_l))).max() <= LSE_ABS
+        # the merged triple of the step range [t0, t1)
+        o, m, l = run_ring(q, k, v, cp, t0, t1, EMIT)
+        rm, rl, ro = OR.ring_attention(qf, kf, vf, scale, cp, steps=range(t0, t1))
+        gm, gl, go = m.cpu().numpy(), l.cpu().numpy(), np.moveaxis(o.cpu().numpy(), 1, 2)
+        ro = np.moveaxis(ro, 1, 2)
+        empty = np.isneginf(rm)
+        assert np.all(np.isneginf(gm[empty])) and np.all(gl[empty] == 0) and np.all(go[empty] == 0)
+        live = ~empty
+        if live.any():
+            assert np.abs(gm[live] - rm[live]).max() <= LSE_ABS
+            assert np.abs(np.log(gl[live]) + gm[live] - np.log(rl[live]) - rm[live]).max() <= LSE_ABS
+            assert_out_close(go[live] / gl[live][:, None], ro[live] / rl[live][:, None], f"steps {t0}-{t1} {case}")
+    finally:
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_PAIRING, 1)
+        cpa.cp_set_kernel_choice(cpa.CP_KNOB_RING_KV_SPLIT, -1)
+
+
 @pytest.mark.parametrize("scale", [0.3, 2.0 / math.sqrt(128)])
 def test_softmax_scale_is_the_one_passed(scale):
     # The scale is an explicit argument: a kernel that used 1/sqrt(d) regardless would
