@@ -429,7 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K::kBarOff);
   // barrier slots
-  const uint32_t bar_q = smem_u32(&bars[0]);
+  const uint32_t bar_q = smem_u32(&bars[0]);  // Q of tile A
+  const uint32_t bar_qb = smem_u32(&bars[16 + 2 * K::kStages]);  // Q of tile B (d = 64)
+  constexpr bool kQSplit = D == 64;
   auto bar_full = [&](int s) { return smem_u32(&bars[1 + s]); };
   auto bar_empty = [&](int s) { return smem_u32(&bars[1 + K::kStages + s]); };
   auto bar_s = [&](int tt) { return smem_u32(&bars[1 + 2 * K::kStages + tt]); };
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(bar_qb, 1);
     for (int s = 0; s < K::kStages; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
@@ -558,11 +561,22 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       // L2 policy: a Q tile is read by this CTA alone, while every query tile of the
       // kv head re-reads its K/V tiles, so K/V should outlive Q (and O) in L2.
       const uint64_t pol_once = l2_policy_evict_first();
-      mbar_expect_tx(bar_q, uint32_t(n_q * K::kTileBytes));
-      for (int tt = 0; tt < n_q; ++tt)
+      // d = 64: Q of tile A, then K_0, then Q of tile B (right after K_0 in the loop below),
+      // so tile A's first QK^T can start before tile B's Q is in.  d = 128: both Q tiles
+      // first, on one barrier.
+      auto load_q = [&](int tt) {
+        const uint32_t bar = (kQSplit && tt == 1) ? bar_qb : bar_q;
         for (int sl = 0; sl < K::kSlabs; ++sl)
-          tma_load_4d_hint(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar_q, sl * 64,
+          tma_load_4d_hint(sbase + K::kQOff + tt * K::kTileBytes + sl * K::kSlab, &p.tmap_q, bar, sl * 64,
                            it.h0 + tt * it.dh, it.q_row0 + tt * it.drow, it.bi, pol_once);
+      };
+      if constexpr (kQSplit) {
+        mbar_expect_tx(bar_q, uint32_t(K::kTileBytes));
+        load_q(0);
+      } else {
+        mbar_expect_tx(bar_q, uint32_t(n_q * K::kTileBytes));
+        for (int tt = 0; tt < n_q; ++tt) load_q(tt);
+      }
       KvCursor<LAYOUT> cur;
       cur.init(p.cp, it.r, it.c_q, p.step_begin, p.step_end, p.C, it.q_last);
       int32_t key0, key_end;
@@ -605,6 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
           for (int sl = 0; sl < K::kSlabs; ++sl)
             tma_load_4d_hint(sbase + K::kKvOff + s * K::kTileBytes + sl * K::kSlab, map, bar_full(s), sl * 64,
                              it.kvh, key0, it.bi, l2_policy_evict_last());
+          if (kQSplit && li == 0 && n_q == 2) {
+            mbar_expect_tx(bar_qb, uint32_t(K::kTileBytes));
+            load_q(1);
+          }
         }
       }
       if (ok && !prefetched) prefetch_old();
@@ -699,11 +717,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
         if (ok) ok = wait(bar_full(0), 0);
         if (ok) {
           tc_fence_after();
-          for (int tt = 0; tt < n_q; ++tt) {
+          for (int tt = 0; ok && tt < n_q; ++tt) {
+            if (kQSplit && tt == 1 && !(ok = wait(bar_qb, 0))) break;
             issue_s(tt, 0);
             mma_commit_if(is, bar_s(tt));
           }
-          mma_commit_if(is, bar_empty(0));
+          if (ok) mma_commit_if(is, bar_empty(0));
         }
         for (int32_t j = 0; ok && j < n_kv; ++j) {
           const int lv = 2 * j + 1, lk = 2 * j + 2;
@@ -731,11 +750,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attn_kernel(const __grid_con
       if (ok) ok = wait(bar_full(0), 0);
       if (ok) {
         tc_fence_after();
-        for (int tt = 0; tt < n_q; ++tt) {
+        for (int tt = 0; ok && tt < n_q; ++tt) {
+          if (kQSplit && tt == 1 && !(ok = wait(bar_qb, 0))) break;
           issue_s(tt, 0);
           mma_commit_if(is, bar_s(tt));
         }
-        mma_commit_if(is, bar_empty(0));
+        if (ok) mma_commit_if(is, bar_empty(0));
       }
       for (int32_t j = 0; ok && j < n_kv; ++j) {
         const int lv = 2 * j + 1, lk = 2 * j + 2;
