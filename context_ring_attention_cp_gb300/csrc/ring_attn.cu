@@ -35,11 +35,19 @@
 //   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane issues)
 //   warps 4-7   softmax of query tile A (thread = row = TMEM lane)
 //   warps 8-11  softmax of query tile B
-// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B.  P (bf16)
-// is written over the first 64 columns of its S tile and fed to the PV MMA from
-// TMEM.  The MMA warp issues PV_T(j) before S_T(j+1), and tcgen05.mma executes in
-// issue order, so P_T(j) is consumed before S_T(j+1) overwrites it.  The commit
-// that signals S_T(j+1) also covers PV_T(j), so softmax may rescale O_T then.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D), O_B.  At d = 128
+// P (bf16) is written over the first 64 columns of its S tile and fed to the PV MMA
+// from TMEM.  The MMA warp issues PV_T(j) before S_T(j+1), and tcgen05.mma executes
+// in issue order, so P_T(j) is consumed before S_T(j+1) overwrites it.  The commit
+// that signals S_T(j+1) also covers PV_T(j), so softmax may rescale O_T then.  At
+// d = 64 P_A, P_B have columns of their own, [384,448) and [448,512): S_T(j+1) is
+// issued as soon as the softmax has read S_T(j), and the softmax waits for PV_T(j-1)
+// before it stores P or rescales O.  A launch of few single query tiles splits each
+// tile's key walk over a cluster of CTAs instead (three S buffers, see below).
+//
+// A launch with CP_MODE_OVERLAP_PREVIOUS is a programmatic dependent of the kernel
+// before it: its CTAs may start in that kernel's tail and touch (o, m, l) only after
+// griddepcontrol.wait.
 //
 // Softmax runs in base 2 on logits scaled by scale*log2(e).  The reference max
 // used for the exponent is only raised when the row max grows by more than 8
