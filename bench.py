@@ -82,6 +82,16 @@ def merge_bytes(w):
 RING_TRAFFIC = {"sha256_prefix": "00629399275168dc", "bytes": 891984640}
 
 
+def headline_config(world):
+    """The headline workload's config, the same object on both arms of the benchmark."""
+    from context_ring_attention_cp_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    return {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
+            "b": w["b"], "S": w["S"], "h_q": w["h_q"], "h_kv": w["h_kv"], "d": w["d"], "cp": w["cp"],
+            "l2": "inputs (402 MB) larger than L2; no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def ring_traffic():
     import hashlib
     path = os.path.join(ROOT, "context_ring_attention_cp_gb300", "csrc", "ring_attn.cu")
@@ -521,11 +531,8 @@ def bench_ours(args, rank, world, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V)",
-            "config": {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
-                       "b": b, "S": S, "h_q": hq, "h_kv": hkv, "d": d, "cp": cp,
-                       "step": "plan + one ring launch over all cp steps (merge fused, finalised) + byte counts",
-                       "l2": "inputs (402 MB) larger than L2; no flush",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": headline_config(world),
+            "step": "plan + one ring launch over all cp steps (merge fused, finalised) + byte counts",
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clocks, "secondary": secondary}
     return line
@@ -822,8 +829,7 @@ def bench_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V)",
-            "config": {"workload": "prefill ring attention, GQA: b1, 32 q / 8 kv heads, d128, S32768, cp8",
-                       "b": w["b"], "S": w["S"], "h_q": w["h_q"], "h_kv": w["h_kv"], "d": w["d"], "cp": w["cp"]},
+            "config": headline_config(world),
             "cpu_baseline": cpu,
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
