@@ -553,30 +553,38 @@ def secondary_lines(cpa, synth, peaks, stream, pool=None):
     m = torch.empty((w["b"], w["h_q"], w["S"]), dtype=torch.float32, device="cuda")
     l = torch.empty_like(m)
     desc = cpa.make_desc(w["b"], w["S"], w["h_q"], w["h_kv"], w["d"], w["cp"], 1.0 / math.sqrt(w["d"]), 1)
-    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, cpa.CP_MODE_EMIT, stream)  # noqa
-    for _ in range(3):
-        fn()
-    ms = _events_time(fn, 20, stream)
+    ovl = cpa.CP_MODE_OVERLAP_PREVIOUS
     C = w["S"] // (2 * w["cp"])
     step_flops = 4 * w["b"] * w["h_q"] * w["d"] * w["cp"] * 2 * C * C
+
+    def one_step(mode):
+        # the step launched 20 times in a row; and the same with every launch a programmatic
+        # dependent of the one before (CP_MODE_OVERLAP_PREVIOUS), as a rank's stream of steps
+        fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, mode, stream)  # noqa
+        fo = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, mode | ovl, stream)  # noqa
+        for _ in range(3):
+            fn()
+            fo()
+        ms = _events_time(fn, 20, stream)
+        ms_o = _events_time(fo, 20, stream)
+        return ms, {"ms": round(ms_o, 4), "value": round(step_flops / (ms_o * 1e-3) / 1e12, 1)}
+
+    ms, overlapped = one_step(cpa.CP_MODE_EMIT)
     tf = step_flops / (ms * 1e-3) / 1e12
     out["prefill_one_step_emit"] = {
         "workload": "one ring step (t=1, all 8 virtual ranks, EMIT) of the GQA prefill workload",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
-        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4), "overlapped": overlapped}
     # the same step merged into a running triple (what every step after the first does
     # when each rank launches per step): O, m and l are read as well as written
     cpa.cp_ring_step_partial_attn(desc, 0, 1, q, k, v, o, m, l, cpa.CP_MODE_EMIT, stream)
-    fn = lambda: cpa.cp_ring_step_partial_attn(desc, 1, 2, q, k, v, o, m, l, cpa.CP_MODE_ACCUMULATE, stream)  # noqa
-    for _ in range(3):
-        fn()
-    ms = _events_time(fn, 20, stream)
+    ms, overlapped = one_step(cpa.CP_MODE_ACCUMULATE)
     tf = step_flops / (ms * 1e-3) / 1e12
     out["prefill_one_step_accumulate"] = {
         "workload": "one ring step (t=1, all 8 virtual ranks, ACCUMULATE into the step-0 triple) "
                     "of the GQA prefill workload",
         "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4), "flops": step_flops,
-        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4)}
+        "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4), "overlapped": overlapped}
     # the whole ring as cp launches of one step each (the first EMIT, then ACCUMULATE, the
     # last normalising), as the steps run when each rank launches per step; each launch a
     # programmatic dependent of the one before (its CTAs start in the previous launch's
